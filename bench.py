@@ -1,0 +1,424 @@
+"""Benchmark: the synthetic drafter layer chain on GB300, one JSON line.
+
+One step = one pass of the whole hot path: 3 drafter layers, each a decode GEMM
+[16, 7168] -> [16, 18432], a decode GEMM [16, 18432] -> [16, 7168] into slot 0 of
+the [8, 16, 7168] partial rows, and reduce + residual + RMSNorm over the 8 slots.
+Metric: achieved HBM GB/s = algorithmic bytes of the step / step time. The
+weights (1.585 GB) are far larger than L2 (~126 MB), so every step streams them
+from HBM; nothing is flushed in between.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (oracle/, test infrastructure) on a bounded
+sample of the same workload on the host cores. N > 1 (torchrun, one rank per GPU)
+runs independent replicas: the path has no exchange step on one node.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "achieved HBM GB/s (and % of GB300 peak) for decode GEMM and reduce+RMSNorm"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_gemm_traffic.json")
+GEMM_SOURCES = ["skinny_bf16_gemm_gb300/csrc/decode_gemm.cu", "skinny_bf16_gemm_gb300/csrc/ptx.cuh",
+                "skinny_bf16_gemm_gb300/csrc/plan.cuh"]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--pdl", type=int, default=1, help="programmatic dependent launch")
+    ap.add_argument("--graph", type=int, default=0, help="replay the step as a CUDA graph")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_info():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def workload_config(cfg, extra=None):
+    c = {"workload": "synthetic drafter layer chain (3 layers: 16x7168->18432 GEMM, "
+                     "16x18432->7168 GEMM, reduce+residual+RMSNorm TP=8 M=16)",
+         "layers": cfg.layers, "M": cfg.M, "hidden": cfg.hidden, "ffn": cfg.ffn, "TP": cfg.TP,
+         "weight_bytes": cfg.weight_bytes(), "step_bytes": cfg.step_bytes(),
+         "l2_policy": "inputs larger than L2 (1.585 GB of weights streamed per step)"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def gemm_source_hash():
+    h = hashlib.sha256()
+    for rel in GEMM_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(shape_key):
+    """DRAM bytes per launch of the decode GEMM from the committed ncu summary,
+    or None if absent or taken on a different version of the kernel."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f)
+    except Exception:
+        return None
+    if t.get("source_hash") != gemm_source_hash():
+        return None
+    entry = t.get("per_launch_bytes", {}).get(shape_key)
+    return None if entry is None else float(entry)
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---- the oracle as the CPU baseline / reference arm ------------------------------
+
+def oracle_chain_sample(inp_bits, cfg, cols1, cols2, threads=0):
+    """One chain step by the oracle on sampled GEMM output columns. The reduce and
+    RMSNorm run on full rows; the sampled columns of GEMM2 fill slot 0 where
+    computed (the rest of slot 0 keeps the previous values). Returns the
+    algorithmic bytes the sample covers."""
+    import oracle
+    x = inp_bits["x0"]
+    res = inp_bits["res0"]
+    M, H, F = cfg.M, cfg.hidden, cfg.ffn
+    h1 = np.zeros((M, F), dtype=np.uint16)
+    slot0 = np.zeros((M, H), dtype=np.uint16)
+    nbytes = 0
+    for l in range(cfg.layers):
+        W1 = inp_bits["W1"][l]
+        W2 = inp_bits["W2"][l]
+        h1[:, cols1] = oracle.decode_gemm(x, W1[cols1], cols=np.arange(len(cols1)), threads=threads)
+        slot0[:, cols2] = oracle.decode_gemm(h1, W2[cols2], cols=np.arange(len(cols2)),
+                                             threads=threads)
+        p = np.concatenate([slot0[None], inp_bits["peers"][l]], axis=0)
+        out, res = oracle.reduce_residual_rmsnorm(p, res, inp_bits["gamma"][l], cfg.eps)
+        x = out
+        nbytes += (2 * len(cols1) * H + 2 * M * H + 2 * M * len(cols1)
+                   + 2 * len(cols2) * F + 2 * M * F + 2 * M * len(cols2)
+                   + cfg.reduce().algorithmic_bytes())
+    return nbytes
+
+
+def host_chain_bits(cfg, seed):
+    """Chain inputs as BF16 patterns on the host, from the seeded generator."""
+    inp = workloads.chain_inputs(cfg, seed, device="cpu")
+    return {"W1": [workloads.bits(w) for w in inp.W1], "W2": [workloads.bits(w) for w in inp.W2],
+            "peers": [workloads.bits(p) for p in inp.peers],
+            "gamma": [workloads.bits(g) for g in inp.gamma],
+            "x0": workloads.bits(inp.x0), "res0": workloads.bits(inp.residual0)}
+
+
+def time_oracle(cfg, budget_s, steps=None, warmup=0, seed=0):
+    """Time the oracle on the chain workload on the host cores.
+
+    Each step covers sampled GEMM output columns sized to about budget_s of CPU
+    work (all columns if a whole step fits). steps=None: repeat steps until about
+    budget_s has elapsed in total (at least one)."""
+    import oracle
+    from oracle import build as obuild
+    obuild.build()
+    bits = host_chain_bits(cfg, seed)
+    threads = oracle.max_threads()
+    probe = 64
+    t0 = time.perf_counter()
+    oracle_chain_sample(bits, cfg, np.arange(probe), np.arange(probe), threads)
+    per_col = (time.perf_counter() - t0) / probe
+    n = int(max(16, budget_s / max(per_col, 1e-9)))
+    rng = np.random.default_rng(seed)
+    cols1 = np.sort(rng.choice(cfg.ffn, size=min(cfg.ffn, n), replace=False)).astype(np.int32)
+    cols2 = np.sort(rng.choice(cfg.hidden, size=min(cfg.hidden, n), replace=False)).astype(np.int32)
+    for _ in range(warmup):
+        oracle_chain_sample(bits, cfg, cols1, cols2, threads)
+    done, nbytes = 0, 0
+    t0 = time.perf_counter()
+    while True:
+        nbytes += oracle_chain_sample(bits, cfg, cols1, cols2, threads)
+        done += 1
+        dt = time.perf_counter() - t0
+        if (steps is not None and done >= steps) or (steps is None and dt >= budget_s):
+            break
+    sample = (f"{len(cols1)} of {cfg.ffn} GEMM1 and {len(cols2)} of {cfg.hidden} GEMM2 output "
+              f"columns per layer (oracle FP64 dot products), full reduce+RMSNorm rows, "
+              f"{cfg.layers} layers per step; {done} step(s) in {dt:.1f} s")
+    return {"value": nbytes / dt / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": sample, "seconds": dt, "steps": done}
+
+
+def run_reference(args, rank, world, cfg):
+    if rank != 0:
+        return 0
+    total = max(1, args.steps + args.warmup)
+    budget = max(0.02, min(10.0, 150.0 / total))
+    r = time_oracle(cfg, budget, steps=max(1, args.steps), warmup=args.warmup)
+    line = {"metric": METRIC, "value": r["value"], "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * r["seconds"] / r["steps"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "impl": "reference", "config": workload_config(cfg),
+            "cpu_baseline": {"value": r["value"], "unit": UNIT, "cores": r["cores"],
+                             "kind": "oracle", "sample": r["sample"]},
+            "e2e": {"value": r["value"], "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---- our arm ------------------------------------------------------------------------
+
+def main():
+    args = parse()
+    rank, world, local = dist_info()
+    cfg = workloads.CHAIN
+    if args.impl == "reference":
+        return run_reference(args, rank, world, cfg)
+
+    import __graft_entry__
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+        if rank == 0:
+            __graft_entry__.build()
+        dist.barrier()
+    else:
+        torch.cuda.set_device(local)
+        __graft_entry__.build()
+    import skinny_bf16_gemm_gb300 as sk
+    from skinny_bf16_gemm_gb300.chain import LayerChain
+
+    device = torch.device("cuda", local)
+    inp = workloads.chain_inputs(cfg, workloads.seed_for("chain", rank), device=device)
+    chain = LayerChain(inp.W1, inp.W2, inp.peers, inp.gamma, cfg.M, cfg.eps, device=device)
+    chain.x.copy_(inp.x0)
+    chain.res_in.copy_(inp.residual0)
+    sk.set_pdl(bool(args.pdl))
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def step():
+        return chain.replay() if chain.graph is not None else chain.run()
+
+    # Warm-up (eager), then optionally capture the step as one graph.
+    for _ in range(max(args.warmup, 3)):
+        chain.run()
+    torch.cuda.synchronize()
+    if args.graph:
+        chain.capture(pdl=bool(args.pdl))
+        for _ in range(3):
+            chain.replay()
+        torch.cuda.synchronize()
+    st, word = sk.device_error(local)
+    if st != 0:
+        raise RuntimeError(f"device error word {word} during warm-up")
+
+    # ---- timed region: K steps, inputs resident ----
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clock_info = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+    value = world * cfg.step_bytes() / (ms_per_step * 1e-3) / 1e9
+    st, word = sk.device_error(local)
+    if st != 0:
+        raise RuntimeError(f"device error word {word} in the timed region")
+
+    # ---- per-kernel durations: the same steps, each launch bracketed by events ----
+    kernel_steps = max(1, min(args.steps, 200))
+    marks = []
+
+    def on_launch(kind, layer, phase):
+        ev = torch.cuda.Event(enable_timing=True)
+        ev.record(stream)
+        marks.append((kind, phase, ev))
+
+    sk.set_pdl(False)  # events between kernels serialise them anyway
+    torch.cuda.synchronize()
+    for _ in range(kernel_steps):
+        chain.run(on_launch=on_launch)
+    torch.cuda.synchronize()
+    sk.set_pdl(bool(args.pdl))
+    dur = {"gemm": [], "reduce": []}
+    for i in range(0, len(marks), 2):
+        kind, _, a = marks[i]
+        _, _, b = marks[i + 1]
+        dur[kind].append(a.elapsed_time(b))
+    gemm_ms = statistics.mean(dur["gemm"])
+    reduce_ms = statistics.mean(dur["reduce"])
+    g1 = cfg.gemm1()
+    gemm_bytes = g1.algorithmic_bytes()  # GEMM1 and GEMM2 move the same bytes
+    peak, peak_kind = measured_peaks()
+    achieved = gemm_bytes / (gemm_ms * 1e-3) / 1e9
+    traffic = recorded_traffic("chain_gemm")
+
+    # ---- end to end through the public API: host inputs in, host result out ----
+    pin = dict(pin_memory=True)
+    host_x = inp.x0.cpu().pin_memory()
+    host_res = inp.residual0.cpu().pin_memory()
+    host_peers = [p.cpu().pin_memory() for p in inp.peers]
+    host_out = torch.empty(cfg.M, cfg.hidden, dtype=torch.bfloat16, **pin)
+    host_res_out = torch.empty(cfg.M, cfg.hidden, dtype=torch.bfloat16, **pin)
+    h2d = (host_x.numel() + host_res.numel() + sum(p.numel() for p in host_peers)) * 2
+    d2h = (host_out.numel() + host_res_out.numel()) * 2
+    e2e_steps = max(1, min(args.steps, 500))
+
+    def e2e_step():
+        chain.x.copy_(host_x, non_blocking=True)
+        chain.res_in.copy_(host_res, non_blocking=True)
+        for l in range(cfg.layers):
+            chain.partials[l][1:].copy_(host_peers[l], non_blocking=True)
+        out, res = chain.run()
+        host_out.copy_(out, non_blocking=True)
+        host_res_out.copy_(res, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    e2e_value = world * cfg.step_bytes() / (e2e_ms * 1e-3) / 1e9
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) activations, N(0,1/K) weights)",
+        "impl": "ours",
+        "config": workload_config(cfg, {"pdl": bool(args.pdl), "graph": bool(args.graph),
+                                        "parallelism": "replicas" if world > 1 else "single"}),
+        "hbm_frac_of_measured": value / peak,
+        "hbm_frac_of_nominal_8000": value / 8000.0,
+        "roofline": {"bound": "hbm", "kernel": "decode_gemm_bf16 (chain shapes)",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6800 GB/s",
+                     "algorithmic_bytes_per_launch": gemm_bytes,
+                     "avg_launch_ms": gemm_ms, "launches_timed": len(dur["gemm"])},
+        "kernels": {"decode_gemm_avg_us": gemm_ms * 1e3, "reduce_rmsnorm_avg_us": reduce_ms * 1e3,
+                    "reduce_algorithmic_bytes": cfg.reduce().algorithmic_bytes(),
+                    "reduce_gbs": cfg.reduce().algorithmic_bytes() / (reduce_ms * 1e-3) / 1e9},
+        "clocks": clock_info,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps * chain.launches_per_step(),
+    }
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = {k: v for k, v in time_oracle(cfg, 10.0).items()
+                                if k in ("value", "unit", "cores", "kind", "sample")}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

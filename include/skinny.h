@@ -1,0 +1,201 @@
+/*
+ * skinny.h -- C ABI of the GB300 (sm_103a) decode GEMM and reduce + residual +
+ * RMSNorm library (libskinny.so).
+ *
+ * Two operations of a speculative-decoding drafter step, as the vLLM DSpark
+ * drafter pages define them:
+ *
+ *   decode_gemm_bf16         out[M,N] = x[M,K] @ W[N,K]^T, BF16 operands, FP32
+ *                            accumulation, one BF16 rounding
+ *                            ("drafter/linears": module text, DraftGemm).
+ *   reduce_residual_rmsnorm  TP BF16 partial rows summed in FP32 in rank order,
+ *                            rounded once; residual added, rounded once; RMSNorm
+ *                            of the result ("drafter/comm": module text, ArNorm;
+ *                            "cutedsl/common/twoshot": reduce, whose one-GPU
+ *                            stand-in lets TP local slots play the ranks).
+ *
+ * Conventions for every entry point below:
+ *  - Pointers are DEVICE pointers (memory of the current CUDA device, from
+ *    cudaMalloc / a PyTorch CUDA tensor) unless a comment says otherwise. The
+ *    caller owns every buffer; the library keeps no pointer after a call returns.
+ *  - BF16 values are IEEE bfloat16 (uint16 bit patterns in memory).
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream). Work is
+ *    enqueued on it; the call returns without waiting for the GPU.
+ *  - Return value: SKINNY_OK (0) or a skinny_status code. On any nonzero code
+ *    nothing was launched and no output was touched. Faults of the GPU work
+ *    itself surface later, at a stream synchronisation, as CUDA errors; a
+ *    kernel whose internal wait ran out instead records a code that
+ *    skinny_device_error() returns.
+ *  - Nothing is allocated per call. decode_gemm_bf16 uses a per-device scratch
+ *    area (split-K partial sums, tile counters, an error word) that its first
+ *    call on each device allocates with cudaMalloc; make that first call outside
+ *    CUDA stream capture. Calls on one device whose kernels may overlap in time
+ *    (unordered streams) share that scratch and must not be issued.
+ *  - Calls are thread-safe on the host.
+ */
+#ifndef SKINNY_H
+#define SKINNY_H
+
+#include <stddef.h>
+
+#if defined(__GNUC__)
+#define SKINNY_API __attribute__((visibility("default")))
+#else
+#define SKINNY_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SKINNY_OK = 0,
+    SKINNY_ERR_NULL = 1,     /* a required pointer is NULL */
+    SKINNY_ERR_SHAPE = 2,    /* a size is outside the accepted range */
+    SKINNY_ERR_ALIGN = 3,    /* a pointer is not aligned as required */
+    SKINNY_ERR_DEVICE = 4,   /* no sm_103 device, or a pointer is not memory of it */
+    SKINNY_ERR_LAUNCH = 5,   /* the CUDA launch itself failed */
+    SKINNY_ERR_ALIAS = 6,    /* an output overlaps an input or the other output */
+    SKINNY_ERR_CAPTURE = 7,  /* first call on a device made during stream capture */
+    SKINNY_ERR_ALLOC = 8,    /* the one-time scratch allocation failed */
+    SKINNY_ERR_TIMEOUT = 9,  /* a kernel's bounded internal wait ran out */
+    SKINNY_ERR_ARG = 10      /* a scalar argument is invalid (eps, timeout, ...) */
+} skinny_status;
+
+/* Row width of every reduce + RMSNorm row: 7168 ("drafter/comm", ArNorm:
+ * "All-reduce of BF16 rows [M, 7168]"; the mean divides by 7168). */
+#define SKINNY_HIDDEN 7168
+/* Largest row count of decode_gemm_bf16 ("drafter/linears" module text: the
+ * stream stays near HBM speed "up to 32 rows"). */
+#define SKINNY_GEMM_MAX_M 32
+/* Largest row count of reduce_residual_rmsnorm (the row cap of the pages'
+ * reduction buffers, "cutedsl/common/twoshot", TwoShot: cap=64). */
+#define SKINNY_REDUCE_MAX_M 64
+/* Largest TP (number of partial slots) of reduce_residual_rmsnorm (TP8 on the
+ * pages, "drafter/comm" module text). */
+#define SKINNY_REDUCE_MAX_TP 8
+
+/*
+ * decode_gemm_bf16 -- out[M,N] = x[M,K] @ W[N,K]^T
+ *   ("drafter/linears": module text, "Precision: BF16 operands, FP32
+ *    accumulation, one BF16 rounding, as cuBLAS; only the summation order
+ *    differs"; DraftGemm: out[M, N] = x[M, K] @ weight[N, K]^T.)
+ *
+ *   x    [M, K] BF16, row-major (row stride K elements), 16-byte aligned.
+ *   W    [N, K] BF16, row-major (each weight row is one output column), 16-byte
+ *        aligned. Read exactly once from HBM.
+ *   out  [M, N] BF16, row-major (row stride N elements), 2-byte aligned. Written
+ *        once; must not overlap x or W.
+ *   1 <= M <= 32;  N >= 1;  K >= 8 and K % 8 == 0 (16-byte row strides).
+ *   Ragged N (N % 128 != 0) and ragged K (K % 64 != 0) are handled exactly.
+ *
+ *   Every out element is the FP32 sum of the K products (split over K across
+ *   CTAs, partial sums added in K order), rounded once to BF16 (nearest even).
+ *   Deterministic: the same inputs on the same device give the same bits.
+ *   Errors: SKINNY_ERR_NULL, _SHAPE, _ALIGN, _ALIAS, _DEVICE, _CAPTURE, _ALLOC,
+ *   _LAUNCH as above.
+ */
+SKINNY_API int decode_gemm_bf16(const void *x, const void *W, void *out,
+                     int M, int N, int K, void *stream);
+
+/*
+ * reduce_residual_rmsnorm -- the ArNorm row operation on TP local slots
+ *   ("drafter/comm": module text -- "summed in FP32 in rank order 0 .. TP-1 and
+ *    rounded once to BF16 ..., the residual is added (one BF16 rounding) and the
+ *    RMSNorm of the new residual follows (FP32 sum of squares, rsqrt(sum / 7168
+ *    + eps), x * rstd * w rounded once)"; ArNorm docstring for the argument list
+ *    and "residual False: the new residual is the all-reduced row itself";
+ *    "cutedsl/common/twoshot": owners = 1 as the one-GPU stand-in, TP local slots
+ *    playing the ranks.)
+ *
+ *   partials      [TP, M, 7168] BF16, contiguous (slot r = rank r's partial row),
+ *                 16-byte aligned.
+ *   residual      [M, 7168] BF16 or NULL (NULL: residual_out = the rounded sum).
+ *   gamma         [7168] BF16, the RMSNorm weight.
+ *   out           [M, 7168] BF16: RMSNorm(residual_out) * gamma.
+ *   residual_out  [M, 7168] BF16: the new residual. May be the same pointer as
+ *                 residual (in-place update); no other overlap between outputs
+ *                 and inputs, or between the two outputs, is allowed.
+ *   All pointers 16-byte aligned. 1 <= TP <= 8; 1 <= M <= 64; eps > 0, finite.
+ *
+ *   residual_out is bit-exact: s = p[0]; s = s + p[r] (FP32, r = 1..TP-1);
+ *   a = BF16(s); h = residual ? BF16(a + residual) : a.
+ *   out = BF16((h * rstd) * gamma), rstd = rsqrt(sum(h^2) / 7168 + eps), FP32.
+ *   Errors: SKINNY_ERR_NULL, _SHAPE, _ALIGN, _ALIAS, _ARG, _DEVICE, _LAUNCH.
+ */
+SKINNY_API int reduce_residual_rmsnorm(const void *partials, int TP, const void *residual,
+                            const void *gamma, void *out, void *residual_out,
+                            int M, float eps, void *stream);
+
+/* Human-readable text of a skinny_status code (static storage). */
+SKINNY_API const char *skinny_status_string(int status);
+
+/*
+ * skinny_device_error -- read and clear the error word of `device`
+ *   Synchronises the device, then returns SKINNY_OK if no kernel of this library
+ *   recorded a problem since the last read, else SKINNY_ERR_TIMEOUT, and writes
+ *   the raw word (a bit set per waiting role that gave up) to *word if word is
+ *   not NULL. Clearing also re-arms the decode GEMM's scratch counters, so the
+ *   next call starts clean. Host pointer: word.
+ */
+SKINNY_API int skinny_device_error(int device, int *word);
+
+/*
+ * skinny_set_pdl -- programmatic dependent launch (PDL) for later launches.
+ *   enable != 0: kernels are launched with programmatic stream serialisation, so
+ *   a kernel may start while its predecessor on the stream finishes. Each kernel
+ *   then reads only data that belongs to the model -- the weight W of
+ *   decode_gemm_bf16, gamma of reduce_residual_rmsnorm -- before waiting for its
+ *   predecessor, and everything else after ("drafter/comm", ArNorm.kernel: gamma
+ *   is loaded before the launch_dependents / wait pair, the rows after it). So
+ *   with PDL on, W and gamma must not be written by the kernel just before the
+ *   call on the same stream. Off by default. Returns the previous setting.
+ */
+SKINNY_API int skinny_set_pdl(int enable);
+
+/* ---- host-side planning (no GPU needed) ------------------------------------ */
+
+/* How decode_gemm_bf16 splits a problem over `num_sms` CTAs (stream-K: the
+ * ceil(N/128) x ceil(K/64) weight blocks, in tile-major order, are cut into
+ * `ctas` contiguous, equal-as-possible ranges). */
+typedef struct {
+    int tiles;          /* ceil(N / 128): 128-row weight tiles */
+    int kblocks;        /* ceil(K / 64): 64-wide K blocks per tile */
+    long long blocks;   /* tiles * kblocks */
+    int ctas;           /* CTAs launched: min(num_sms, blocks) */
+    int mma_n;          /* padded row count the MMA runs with: 16 or 32 */
+    int stages;         /* shared-memory pipeline stages per CTA */
+    int smem_bytes;     /* dynamic shared memory per CTA */
+    int split_tiles;    /* tiles whose K range spans more than one CTA */
+} skinny_gemm_plan;
+
+/* Fill *plan for (M, N, K) on a device with num_sms SMs. Host pointer: plan.
+ * Returns SKINNY_ERR_SHAPE for shapes decode_gemm_bf16 rejects. */
+SKINNY_API int skinny_gemm_plan_query(int M, int N, int K, int num_sms, skinny_gemm_plan *plan);
+
+/* The pieces CTA `cta` of that plan computes: for each of at most max_pieces
+ * pieces, the tile, its K-block range [kb0, kb1), and the scratch slot its
+ * partial sum goes to (-1 for a tile the CTA covers whole). Host pointers.
+ * Returns the number of pieces, or -1 on bad arguments. */
+SKINNY_API int skinny_gemm_cta_pieces(int M, int N, int K, int num_sms, int cta, int *tile,
+                           int *kb0, int *kb1, int *slot, int max_pieces);
+
+/* ---- diagnostics ---------------------------------------------------------- */
+
+/*
+ * skinny_watchdog_selftest -- exercise the decode GEMM's bounded-wait path.
+ *   Launches decode_gemm_bf16's kernel on (x, W, out, M, N, K) with its MMA
+ *   role first waiting on a barrier that nothing ever completes, limited to
+ *   timeout_ns nanoseconds (1e3 <= timeout_ns <= 2e9). The kernel records
+ *   the timeout in the device error word, drains the copies it has in flight,
+ *   frees its tensor memory and exits; out is left unspecified. Read the outcome
+ *   with skinny_device_error(). For tests of the failure path only.
+ */
+SKINNY_API int skinny_watchdog_selftest(const void *x, const void *W, void *out, int M, int N,
+                             int K, long long timeout_ns, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SKINNY_H */

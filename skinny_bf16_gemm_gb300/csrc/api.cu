@@ -1,0 +1,381 @@
+// The library's C ABI (include/skinny.h): argument checks, the per-device state
+// (SM count, split-K scratch, error word), TMA descriptor encoding and launches.
+// Every check runs before any launch; a rejected call touches nothing.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "kernels.h"
+#include "plan.cuh"
+#include "skinny.h"
+
+namespace skinny {
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per internal wait
+
+struct DeviceState {
+    bool ready = false;
+    int sms = 0;
+    int major = 0, minor = 0;
+    // Split-K scratch of the decode GEMM, sized for one CTA per SM.
+    void *scratch = nullptr;
+    float *partials = nullptr;
+    unsigned *counters = nullptr;
+    int *err = nullptr;
+    size_t counter_bytes = 0;
+};
+
+std::mutex g_mutex;
+DeviceState g_devices[kMaxDevices];
+bool g_pdl = false;  // programmatic dependent launch, opt-in (skinny_set_pdl)
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+int current_device(int *dev) {
+    if (cudaGetDevice(dev) != cudaSuccess || *dev < 0 || *dev >= kMaxDevices) {
+        cudaGetLastError();
+        return SKINNY_ERR_DEVICE;
+    }
+    return SKINNY_OK;
+}
+
+// Device properties (once per device). Caller holds g_mutex.
+int device_state_locked(int dev, DeviceState **out) {
+    DeviceState &d = g_devices[dev];
+    if (!d.ready) {
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return SKINNY_ERR_DEVICE;
+        }
+        d.ready = true;
+    }
+    // The kernels are built for sm_103a only.
+    if (d.major != 10 || d.minor != 3) return SKINNY_ERR_DEVICE;
+    *out = &d;
+    return SKINNY_OK;
+}
+
+int device_state(int dev, DeviceState **out) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    return device_state_locked(dev, out);
+}
+
+// The decode GEMM's scratch: allocated and zeroed once per device.
+int ensure_scratch(int dev, cudaStream_t stream, DeviceState **out) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState *d = nullptr;
+    int st = device_state_locked(dev, &d);
+    if (st != SKINNY_OK) return st;
+    if (d->scratch == nullptr) {
+        cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) {
+            cudaGetLastError();
+            return SKINNY_ERR_LAUNCH;
+        }
+        if (cap != cudaStreamCaptureStatusNone) return SKINNY_ERR_CAPTURE;
+        const size_t partial_bytes = static_cast<size_t>(2) * d->sms * kSlotFloats * sizeof(float);
+        const size_t counter_bytes = (static_cast<size_t>(d->sms) * sizeof(unsigned) + 255) / 256 * 256;
+        const size_t bytes = partial_bytes + counter_bytes + 256;
+        void *p = nullptr;
+        if (cudaMalloc(&p, bytes) != cudaSuccess) {
+            cudaGetLastError();
+            return SKINNY_ERR_ALLOC;
+        }
+        if (cudaMemset(p, 0, bytes) != cudaSuccess) {
+            cudaGetLastError();
+            cudaFree(p);
+            return SKINNY_ERR_ALLOC;
+        }
+        d->scratch = p;
+        d->partials = static_cast<float *>(p);
+        d->counters = reinterpret_cast<unsigned *>(static_cast<char *>(p) + partial_bytes);
+        d->err = reinterpret_cast<int *>(static_cast<char *>(p) + partial_bytes + counter_bytes);
+        d->counter_bytes = counter_bytes;
+    }
+    *out = d;
+    return SKINNY_OK;
+}
+
+int encoder(EncodeTiledFn *fn) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (g_encode == nullptr) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || p == nullptr) {
+            cudaGetLastError();
+            return SKINNY_ERR_DEVICE;
+        }
+        g_encode = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    *fn = g_encode;
+    return SKINNY_OK;
+}
+
+// The pointer must be device (or managed) memory of device `dev`.
+int check_device_pointer(const void *p, int dev) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return SKINNY_ERR_DEVICE;
+    }
+    if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged) return SKINNY_ERR_DEVICE;
+    if (a.device != dev) return SKINNY_ERR_DEVICE;
+    return SKINNY_OK;
+}
+
+bool overlaps(const void *a, size_t an, const void *b, size_t bn) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + bn && b0 < a0 + an;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// 2-D BF16 tensor map over a row-major [rows, cols] array, box [box_rows, 64].
+int encode_2d(EncodeTiledFn enc, CUtensorMap *map, const void *base, uint64_t rows,
+              uint64_t cols, uint32_t box_rows) {
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBlockK), box_rows};
+    const cuuint32_t estride[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
+                     strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? SKINNY_OK : SKINNY_ERR_LAUNCH;
+}
+
+int gemm_shape_ok(int M, int N, int K) {
+    if (M < 1 || M > kMaxM || N < 1 || K < 8 || (K % 8) != 0) return SKINNY_ERR_SHAPE;
+    return SKINNY_OK;
+}
+
+int mma_n_for(int M) { return M <= 16 ? 16 : 32; }
+
+int gemm_launch(const void *x, const void *W, void *out, int M, int N, int K, void *stream,
+                int selftest, unsigned long long limit_ns) {
+    if (!x || !W || !out) return SKINNY_ERR_NULL;
+    int st = gemm_shape_ok(M, N, K);
+    if (st) return st;
+    if (!aligned(x, 16) || !aligned(W, 16) || !aligned(out, 2)) return SKINNY_ERR_ALIGN;
+    const size_t xb = static_cast<size_t>(M) * K * 2, wb = static_cast<size_t>(N) * K * 2,
+                 ob = static_cast<size_t>(M) * N * 2;
+    if (overlaps(out, ob, x, xb) || overlaps(out, ob, W, wb)) return SKINNY_ERR_ALIAS;
+    int dev;
+    if ((st = current_device(&dev))) return st;
+    if ((st = check_device_pointer(x, dev)) || (st = check_device_pointer(W, dev)) ||
+        (st = check_device_pointer(out, dev)))
+        return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    DeviceState *d = nullptr;
+    if ((st = ensure_scratch(dev, s, &d))) return st;
+    EncodeTiledFn enc;
+    if ((st = encoder(&enc))) return st;
+    const int mma_n = mma_n_for(M);
+    alignas(64) CUtensorMap w_map, x_map;
+    if ((st = encode_2d(enc, &w_map, W, N, K, kBlockN))) return st;
+    if ((st = encode_2d(enc, &x_map, x, M, K, mma_n))) return st;
+    const GemmGeometry g = make_geometry(M, N, K, d->sms);
+    GemmArgs a;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.out = static_cast<uint16_t *>(out);
+    a.partials = d->partials;
+    a.counters = d->counters;
+    a.err = d->err;
+    a.wait_limit_ns = limit_ns;
+    a.selftest = selftest;
+    bool pdl;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        pdl = g_pdl;
+    }
+    cudaError_t e = launch_decode_gemm(w_map, x_map, a, mma_n, g.ctas, s, pdl, dev);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return SKINNY_ERR_LAUNCH;
+    }
+    return SKINNY_OK;
+}
+
+// CTAs per row of the reduce: enough rows x CTAs to spread a small problem over
+// many SMs, fewer (bigger) CTAs once rows alone fill the GPU.
+int reduce_ctas_per_row(int M) { return M <= 32 ? 8 : 4; }
+
+}  // namespace
+}  // namespace skinny
+
+using namespace skinny;
+
+extern "C" {
+
+int decode_gemm_bf16(const void *x, const void *W, void *out, int M, int N, int K, void *stream) {
+    return gemm_launch(x, W, out, M, N, K, stream, 0, kWaitLimitNs);
+}
+
+int skinny_watchdog_selftest(const void *x, const void *W, void *out, int M, int N, int K,
+                             long long timeout_ns, void *stream) {
+    if (timeout_ns < 1000 || timeout_ns > 2000000000LL) return SKINNY_ERR_ARG;
+    return gemm_launch(x, W, out, M, N, K, stream, 1,
+                       static_cast<unsigned long long>(timeout_ns));
+}
+
+int reduce_residual_rmsnorm(const void *partials, int TP, const void *residual,
+                            const void *gamma, void *out, void *residual_out, int M, float eps,
+                            void *stream) {
+    if (!partials || !gamma || !out || !residual_out) return SKINNY_ERR_NULL;
+    if (TP < 1 || TP > SKINNY_REDUCE_MAX_TP || M < 1 || M > SKINNY_REDUCE_MAX_M)
+        return SKINNY_ERR_SHAPE;
+    if (!(eps > 0.0f) || !std::isfinite(eps)) return SKINNY_ERR_ARG;
+    if (!aligned(partials, 16) || !aligned(gamma, 16) || !aligned(out, 16) ||
+        !aligned(residual_out, 16) || (residual && !aligned(residual, 16)))
+        return SKINNY_ERR_ALIGN;
+    const size_t row = static_cast<size_t>(M) * SKINNY_HIDDEN * 2;
+    const size_t pb = row * TP, gb = SKINNY_HIDDEN * 2;
+    if (overlaps(out, row, residual_out, row) || overlaps(out, row, partials, pb) ||
+        overlaps(out, row, gamma, gb) || overlaps(residual_out, row, partials, pb) ||
+        overlaps(residual_out, row, gamma, gb) || (residual && overlaps(out, row, residual, row)))
+        return SKINNY_ERR_ALIAS;
+    // residual_out may be residual itself (element-wise in-place), nothing else.
+    if (residual && residual != residual_out && overlaps(residual_out, row, residual, row))
+        return SKINNY_ERR_ALIAS;
+    int dev, st;
+    if ((st = current_device(&dev))) return st;
+    DeviceState *d = nullptr;
+    if ((st = device_state(dev, &d))) return st;
+    if ((st = check_device_pointer(partials, dev)) || (st = check_device_pointer(gamma, dev)) ||
+        (st = check_device_pointer(out, dev)) || (st = check_device_pointer(residual_out, dev)) ||
+        (residual && (st = check_device_pointer(residual, dev))))
+        return st;
+    bool pdl;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        pdl = g_pdl;
+    }
+    cudaError_t e = launch_reduce_rmsnorm(partials, TP, residual, gamma, out, residual_out, M, eps,
+                                          reduce_ctas_per_row(M),
+                                          static_cast<cudaStream_t>(stream), pdl);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return SKINNY_ERR_LAUNCH;
+    }
+    return SKINNY_OK;
+}
+
+const char *skinny_status_string(int status) {
+    switch (status) {
+        case SKINNY_OK: return "ok";
+        case SKINNY_ERR_NULL: return "a required pointer is NULL";
+        case SKINNY_ERR_SHAPE: return "a size is outside the accepted range";
+        case SKINNY_ERR_ALIGN: return "a pointer is not aligned as required";
+        case SKINNY_ERR_DEVICE: return "no sm_103 device, or a pointer is not memory of the current device";
+        case SKINNY_ERR_LAUNCH: return "the CUDA launch failed";
+        case SKINNY_ERR_ALIAS: return "an output overlaps an input or the other output";
+        case SKINNY_ERR_CAPTURE: return "first call on this device made during stream capture";
+        case SKINNY_ERR_ALLOC: return "scratch allocation failed";
+        case SKINNY_ERR_TIMEOUT: return "a kernel's bounded internal wait ran out";
+        case SKINNY_ERR_ARG: return "a scalar argument is invalid";
+        default: return "unknown status";
+    }
+}
+
+int skinny_device_error(int device, int *word) {
+    if (device < 0 || device >= kMaxDevices) return SKINNY_ERR_DEVICE;
+    if (word) *word = 0;
+    int prev = -1;
+    if (cudaGetDevice(&prev) != cudaSuccess) {
+        cudaGetLastError();
+        return SKINNY_ERR_DEVICE;
+    }
+    if (cudaSetDevice(device) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        cudaSetDevice(prev);
+        return SKINNY_ERR_DEVICE;
+    }
+    int value = 0;
+    int st = SKINNY_OK;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        DeviceState &d = g_devices[device];
+        if (d.scratch) {
+            if (cudaMemcpy(&value, d.err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) {
+                cudaGetLastError();
+                st = SKINNY_ERR_DEVICE;
+            } else if (value != 0) {
+                // A kernel gave up part-way: clear the word and the tile counters.
+                if (cudaMemset(d.err, 0, sizeof(int)) != cudaSuccess ||
+                    cudaMemset(d.counters, 0, d.counter_bytes) != cudaSuccess) {
+                    cudaGetLastError();
+                    st = SKINNY_ERR_DEVICE;
+                }
+            }
+        }
+    }
+    cudaSetDevice(prev);
+    if (word) *word = value;
+    if (st != SKINNY_OK) return st;
+    return value ? SKINNY_ERR_TIMEOUT : SKINNY_OK;
+}
+
+int skinny_set_pdl(int enable) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    const int prev = g_pdl ? 1 : 0;
+    g_pdl = enable != 0;
+    return prev;
+}
+
+int skinny_gemm_plan_query(int M, int N, int K, int num_sms, skinny_gemm_plan *plan) {
+    if (!plan) return SKINNY_ERR_NULL;
+    if (num_sms < 1) return SKINNY_ERR_ARG;
+    int st = gemm_shape_ok(M, N, K);
+    if (st) return st;
+    const GemmGeometry g = make_geometry(M, N, K, num_sms);
+    plan->tiles = g.tiles;
+    plan->kblocks = g.kblocks;
+    plan->blocks = g.blocks;
+    plan->ctas = g.ctas;
+    plan->mma_n = mma_n_for(M);
+    plan->stages = gemm_stages(plan->mma_n);
+    plan->smem_bytes = gemm_smem_bytes(plan->mma_n);
+    int split = 0;
+    for (int t = 0; t < g.tiles; ++t) {
+        int first, last;
+        tile_contributors(g, t, first, last);
+        split += first != last;
+    }
+    plan->split_tiles = split;
+    return SKINNY_OK;
+}
+
+int skinny_gemm_cta_pieces(int M, int N, int K, int num_sms, int cta, int *tile, int *kb0,
+                           int *kb1, int *slot, int max_pieces) {
+    if (!tile || !kb0 || !kb1 || !slot || num_sms < 1 || gemm_shape_ok(M, N, K)) return -1;
+    const GemmGeometry g = make_geometry(M, N, K, num_sms);
+    if (cta < 0 || cta >= g.ctas) return -1;
+    const int n = cta_piece_count(g, cta);
+    for (int q = 0; q < n && q < max_pieces; ++q) {
+        const Piece p = cta_piece(g, cta, q);
+        tile[q] = p.tile;
+        kb0[q] = p.kb0;
+        kb1[q] = p.kb1;
+        const bool whole = p.kb0 == 0 && p.kb1 == g.kblocks;
+        slot[q] = whole ? -1 : partial_slot(g, cta, p.tile);
+    }
+    return n;
+}
+
+}  // extern "C"

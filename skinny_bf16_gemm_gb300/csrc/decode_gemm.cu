@@ -1,0 +1,420 @@
+// Decode GEMM for GB300 (sm_103a): out[M, N] = x[M, K] @ W[N, K]^T, BF16 operands,
+// FP32 accumulation, one BF16 rounding ("drafter/linears": module text and
+// DraftGemm). M <= 32, so the time is the weight stream: every byte of W is read
+// once from HBM by TMA and fed to the tensor cores while it is on chip.
+//
+// One persistent CTA per SM, 192 threads in three roles:
+//   warp 0      TMA producer: W tiles [128 rows x 64 K] and x slices [MP x 64 K]
+//               into a ring of STAGES shared-memory stages (128-byte swizzle);
+//   warp 1      MMA issuer: tcgen05.mma kind::f16, M = 128 weight rows, N = MP
+//               (x rows padded to 16 or 32; the padding rows are TMA zero fill),
+//               accumulating in tensor memory (two 32-column buffers);
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator (TMEM lane = weight row =
+//               output column n, column = output row m), one BF16 rounding, or
+//               the split-K fix-up.
+// Work split (plan.cuh): the ceil(N/128) x ceil(K/64) weight blocks are dealt to
+// the CTAs as equal contiguous ranges. A tile whose K range is shared by several
+// CTAs is finished by the last to arrive (an atomic counter per tile), which adds
+// all FP32 partial sums in K order, so results do not depend on arrival order.
+// Before waiting on the previous kernel in the stream (programmatic dependent
+// launch) the producer already streams the first STAGES weight tiles: weights
+// never depend on the previous kernel, x may.
+// Every wait is bounded (wait_limit_ns); a role that gives up records a bit in
+// the device error word, the CTA drains its in-flight copies and MMAs, frees its
+// tensor memory and exits.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "kernels.h"
+#include "plan.cuh"
+#include "ptx.cuh"
+
+namespace skinny {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kEpilogueThreads = 128;
+constexpr int kTmemCols = 64;          // two accumulator buffers of 32 columns
+constexpr int kWBytes = kBlockN * kBlockK * 2;
+constexpr uint64_t kDrainLimitNs = 200000000ull;  // 0.2 s for copies already issued
+
+template <int MP>
+struct Layout {
+    static constexpr int kStages = MP == 16 ? 10 : 9;
+    static constexpr int kXBytes = MP * kBlockK * 2;
+    static constexpr int kStageBytes = kWBytes + kXBytes;
+    static constexpr int kBarOffset = kStages * kStageBytes;
+    static constexpr int kNumBars = 2 * kStages + 6;
+    static constexpr int kMiscOffset = kBarOffset + kNumBars * 8;
+    static constexpr int kBytes = kMiscOffset + 16;
+    static constexpr int kDynamicBytes = kBytes + 1024;  // slack to align the base to 1024
+    static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
+};
+
+enum WaitResult { kWaitDone = 1, kWaitTimeout = 0, kWaitAborted = -1 };
+
+// Wait for completion of the barrier phase with `parity`, giving up after
+// limit_ns or as soon as another role of this CTA has aborted.
+__device__ __forceinline__ int bounded_wait(uint32_t bar, uint32_t parity,
+                                            const volatile uint32_t *abort_flag,
+                                            uint64_t limit_ns) {
+    if (ptx::mbar_try_wait(bar, parity)) return kWaitDone;
+    const uint64_t t0 = ptx::global_timer_ns();
+    for (uint32_t spin = 1;; ++spin) {
+        if (ptx::mbar_try_wait(bar, parity)) return kWaitDone;
+        if ((spin & 15u) == 0) {
+            if (*abort_flag) return kWaitAborted;
+            if (ptx::global_timer_ns() - t0 > limit_ns) return kWaitTimeout;
+        }
+    }
+}
+
+__device__ __forceinline__ void raise_error(int *err, volatile uint32_t *abort_flag, int bit) {
+    atomicOr(err, bit);
+    *abort_flag = 1u;
+}
+
+// Barrier-wide OR of a predicate over the epilogue's 128 threads (named barrier 1).
+__device__ __forceinline__ bool epilogue_any(bool p) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred a, b;\n\t"
+        "setp.ne.u32 a, %1, 0;\n\t"
+        "bar.red.or.pred b, 1, 128, a;\n\t"
+        "selp.u32 %0, 1, 0, b;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(p))
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ uint16_t to_bf16_bits(float v) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+}
+
+template <int MP>
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_gemm_kernel(const __grid_constant__ CUtensorMap w_map,
+                       const __grid_constant__ CUtensorMap x_map, const GemmArgs args) {
+    using L = Layout<MP>;
+    constexpr int S = L::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = ptx::smem_addr(smem);
+    const uint32_t bar_full = sbase + L::kBarOffset;   // + 8 s
+    const uint32_t bar_empty = bar_full + 8 * S;       // + 8 s
+    const uint32_t bar_acc_full = bar_empty + 8 * S;   // + 8 b
+    const uint32_t bar_acc_empty = bar_acc_full + 16;  // + 8 b
+    const uint32_t bar_drain = bar_acc_empty + 16;
+    const uint32_t bar_never = bar_drain + 8;
+    volatile uint32_t *misc = reinterpret_cast<volatile uint32_t *>(smem + L::kMiscOffset);
+    // misc[0]: tensor-memory base, misc[1]: abort flag, misc[2]: "last to arrive" flag
+
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    const int cta = blockIdx.x;
+    const GemmGeometry g = make_geometry(args.M, args.N, args.K, gridDim.x);
+    const uint64_t limit = args.wait_limit_ns;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            ptx::mbar_init(bar_full + 8 * s, 1);
+            ptx::mbar_init(bar_empty + 8 * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(bar_acc_full + 8 * b, 1);
+            ptx::mbar_init(bar_acc_empty + 8 * b, kEpilogueThreads);
+        }
+        ptx::mbar_init(bar_drain, 1);
+        ptx::mbar_init(bar_never, 1);
+        misc[1] = 0u;
+        misc[2] = 0u;
+        ptx::fence_barrier_init();
+    }
+    if (warp == 0) {
+        ptx::tmem_alloc(sbase + L::kMiscOffset, kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    ptx::tc_fence_after_sync();
+    const uint32_t tmem_base = misc[0];
+    volatile uint32_t *abort_flag = misc + 1;
+
+    // Dependent kernels may be scheduled now; they wait for this grid before
+    // touching anything it writes.
+    ptx::pdl_launch_dependents();
+
+    const int pieces = cta_piece_count(g, cta);
+    const long long b0 = cta_begin(g, cta);
+    const long long total = cta_begin(g, cta + 1) - b0;
+
+    // Producer bookkeeping kept for the drain (lane 0 of warp 0).
+    uint32_t armed = 0, armed_parity = 0;
+    // MMA bookkeeping for the drain (lane 0 of warp 1).
+    bool mma_issued = false;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer ----------------
+            ptx::prefetch_tensormap(&w_map);
+            ptx::prefetch_tensormap(&x_map);
+            const uint64_t pol_w = ptx::policy_evict_first();
+            const uint64_t pol_x = ptx::policy_evict_last();
+            const int npre = static_cast<int>(total < S ? total : S);
+            // Fresh stages: arm them and stream weights before the predecessor ends.
+            for (int j = 0; j < npre; ++j) {
+                const long long blk = b0 + j;
+                const int t = static_cast<int>(blk / g.kblocks);
+                const int kb = static_cast<int>(blk % g.kblocks);
+                const uint32_t st = sbase + j * L::kStageBytes;
+                ptx::mbar_arrive_expect_tx(bar_full + 8 * j, L::kStageBytes);
+                armed |= 1u << j;
+                ptx::tma_load_2d(st, &w_map, bar_full + 8 * j, kb * kBlockK, t * kBlockN, pol_w);
+            }
+            ptx::pdl_wait();  // x may be the predecessor's output
+            for (int j = 0; j < npre; ++j) {
+                const int kb = static_cast<int>((b0 + j) % g.kblocks);
+                const uint32_t st = sbase + j * L::kStageBytes;
+                ptx::tma_load_2d(st + kWBytes, &x_map, bar_full + 8 * j, kb * kBlockK, 0, pol_x);
+            }
+            int s = npre % S;
+            uint32_t ph = npre == S ? 1u : 0u;
+            for (long long j = npre; j < total; ++j) {
+                const int r = bounded_wait(bar_empty + 8 * s, ph ^ 1u, abort_flag, limit);
+                if (r != kWaitDone) {
+                    if (r == kWaitTimeout) raise_error(args.err, abort_flag, kErrProducerWait);
+                    break;
+                }
+                const long long blk = b0 + j;
+                const int t = static_cast<int>(blk / g.kblocks);
+                const int kb = static_cast<int>(blk % g.kblocks);
+                const uint32_t st = sbase + s * L::kStageBytes;
+                ptx::mbar_arrive_expect_tx(bar_full + 8 * s, L::kStageBytes);
+                armed |= 1u << s;
+                armed_parity = (armed_parity & ~(1u << s)) | (ph << s);
+                ptx::tma_load_2d(st, &w_map, bar_full + 8 * s, kb * kBlockK, t * kBlockN, pol_w);
+                ptx::tma_load_2d(st + kWBytes, &x_map, bar_full + 8 * s, kb * kBlockK, 0, pol_x);
+                if (++s == S) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer ----------------
+            constexpr uint32_t idesc = ptx::idesc_bf16_f32(kBlockN, MP);
+            ptx::pdl_wait();  // start the bounded waits' clocks after the predecessor
+            int s = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            if (args.selftest) {
+                // Wait on a barrier nothing ever completes: exercises the bounded wait.
+                const int r = bounded_wait(bar_never, 0, abort_flag, limit);
+                if (r == kWaitTimeout) raise_error(args.err, abort_flag, kErrSelftest);
+                ok = false;
+            }
+            for (int q = 0; ok && q < pieces; ++q) {
+                const Piece p = cta_piece(g, cta, q);
+                const int b = q & 1;
+                const uint32_t aph = (q >> 1) & 1;
+                int r = bounded_wait(bar_acc_empty + 8 * b, aph ^ 1u, abort_flag, limit);
+                if (r != kWaitDone) {
+                    if (r == kWaitTimeout) raise_error(args.err, abort_flag, kErrMmaAccWait);
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + b * 32;
+                for (int kb = p.kb0; kb < p.kb1; ++kb) {
+                    r = bounded_wait(bar_full + 8 * s, ph, abort_flag, limit);
+                    if (r != kWaitDone) {
+                        if (r == kWaitTimeout) raise_error(args.err, abort_flag, kErrMmaFullWait);
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after_sync();
+                    const uint32_t st = sbase + s * L::kStageBytes;
+                    const uint64_t a_desc = ptx::smem_desc_sw128_kmajor(st);
+                    const uint64_t b_desc = ptx::smem_desc_sw128_kmajor(st + kWBytes);
+#pragma unroll
+                    for (int k = 0; k < kBlockK / 16; ++k) {
+                        // +32 bytes along K per step: +2 in the address field (>> 4).
+                        ptx::mma_bf16(d_tmem, a_desc + 2 * k, b_desc + 2 * k, idesc,
+                                      (kb > p.kb0 || k > 0) ? 1u : 0u);
+                    }
+                    mma_issued = true;
+                    ptx::mma_commit(bar_empty + 8 * s);  // stage free once these MMAs finish
+                    if (++s == S) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                ptx::mma_commit(bar_acc_full + 8 * b);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---------------- epilogue (128 threads) ----------------
+        ptx::pdl_wait();  // scratch and out may still be in use by the predecessor
+        const int quarter = warp & 3;              // TMEM lanes 32*quarter .. +31
+        const int row = quarter * 32 + lane;       // weight row within the tile
+        const int etid = threadIdx.x - 64;
+        for (int q = 0; q < pieces; ++q) {
+            const Piece p = cta_piece(g, cta, q);
+            const int b = q & 1;
+            const uint32_t aph = (q >> 1) & 1;
+            const int r = bounded_wait(bar_acc_full + 8 * b, aph, abort_flag, limit);
+            if (r == kWaitTimeout) raise_error(args.err, abort_flag, kErrEpilogueWait);
+            if (epilogue_any(r != kWaitDone)) break;
+            ptx::tc_fence_after_sync();
+            float acc[MP];
+            {
+                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + b * 32;
+                uint32_t v[16];
+                ptx::tmem_ld16(taddr, v);
+                ptx::tmem_ld_wait(v);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) acc[i] = __uint_as_float(v[i]);
+                if constexpr (MP == 32) {
+                    ptx::tmem_ld16(taddr + 16, v);
+                    ptx::tmem_ld_wait(v);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) acc[16 + i] = __uint_as_float(v[i]);
+                }
+            }
+            ptx::tc_fence_before_sync();
+            ptx::mbar_arrive(bar_acc_empty + 8 * b);  // the MMA may reuse this buffer
+
+            const int n = p.tile * kBlockN + row;
+            const bool in_range = n < g.N;
+            if (p.kb0 == 0 && p.kb1 == g.kblocks) {
+                // Whole tile in this CTA: round once and store.
+                if (in_range) {
+#pragma unroll
+                    for (int m = 0; m < MP; ++m)
+                        if (m < g.M) args.out[static_cast<size_t>(m) * g.N + n] = to_bf16_bits(acc[m]);
+                }
+                continue;
+            }
+            // Shared tile: publish this CTA's partial, count arrivals; the last
+            // arrival adds every partial in K (= CTA) order and stores.
+            int first, last;
+            tile_contributors(g, p.tile, first, last);
+            float *mine = args.partials + static_cast<size_t>(partial_slot(g, cta, p.tile)) * kSlotFloats;
+#pragma unroll
+            for (int m = 0; m < MP; ++m)
+                if (m < g.M) __stcg(mine + m * kBlockN + row, acc[m]);
+            __threadfence();
+            ptx::named_barrier_sync(1, kEpilogueThreads);
+            if (etid == 0) {
+                __threadfence();
+                const unsigned prev = atomicInc(args.counters + first, static_cast<unsigned>(last - first));
+                misc[2] = prev == static_cast<unsigned>(last - first) ? 1u : 0u;
+                __threadfence();
+            }
+            ptx::named_barrier_sync(1, kEpilogueThreads);
+            if (misc[2] != 0u) {
+                __threadfence();
+                if (in_range) {
+#pragma unroll
+                    for (int m = 0; m < MP; ++m) {
+                        if (m >= g.M) continue;
+                        float sum = 0.0f;
+                        for (int c = first; c <= last; ++c) {
+                            const float v = c == cta
+                                                ? acc[m]
+                                                : __ldcg(args.partials +
+                                                         static_cast<size_t>(partial_slot(g, c, p.tile)) * kSlotFloats +
+                                                         m * kBlockN + row);
+                            sum = c == first ? v : __fadd_rn(sum, v);
+                        }
+                        args.out[static_cast<size_t>(m) * g.N + n] = to_bf16_bits(sum);
+                    }
+                }
+            }
+            ptx::named_barrier_sync(1, kEpilogueThreads);  // misc[2] is reused next piece
+        }
+    }
+
+    // ---------------- teardown ----------------
+    __syncthreads();
+    if (*abort_flag) {
+        // Nothing may still write this CTA's shared or tensor memory when it exits.
+        if (warp == 0 && lane == 0) {
+            for (int s = 0; s < S; ++s) {
+                if (!(armed & (1u << s))) continue;
+                const uint32_t par = (armed_parity >> s) & 1u;
+                const uint64_t t0 = ptx::global_timer_ns();
+                while (!ptx::mbar_try_wait(bar_full + 8 * s, par)) {
+                    if (ptx::global_timer_ns() - t0 > kDrainLimitNs) {
+                        atomicOr(args.err, kErrDrain);
+                        break;
+                    }
+                }
+            }
+        }
+        if (warp == 1 && lane == 0 && mma_issued) {
+            ptx::mma_commit(bar_drain);
+            const uint64_t t0 = ptx::global_timer_ns();
+            while (!ptx::mbar_try_wait(bar_drain, 0)) {
+                if (ptx::global_timer_ns() - t0 > kDrainLimitNs) {
+                    atomicOr(args.err, kErrDrain);
+                    break;
+                }
+            }
+        }
+        __syncthreads();
+    }
+    if (warp == 0) {
+        ptx::tc_fence_after_sync();
+        ptx::tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+template <int MP>
+cudaError_t launch_mp(const CUtensorMap &w_map, const CUtensorMap &x_map, const GemmArgs &args,
+                      int ctas, cudaStream_t stream, bool pdl, int device) {
+    static bool configured[64] = {};
+    if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+    if (!configured[device]) {
+        cudaError_t e = cudaFuncSetAttribute(decode_gemm_kernel<MP>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             Layout<MP>::kDynamicBytes);
+        if (e != cudaSuccess) return e;
+        configured[device] = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ctas, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = Layout<MP>::kDynamicBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, decode_gemm_kernel<MP>, w_map, x_map, args);
+}
+
+}  // namespace
+
+int gemm_stages(int mma_n) { return mma_n == 16 ? Layout<16>::kStages : Layout<32>::kStages; }
+
+int gemm_smem_bytes(int mma_n) {
+    return mma_n == 16 ? Layout<16>::kDynamicBytes : Layout<32>::kDynamicBytes;
+}
+
+cudaError_t launch_decode_gemm(const CUtensorMap &w_map, const CUtensorMap &x_map,
+                               const GemmArgs &args, int mma_n, int ctas, cudaStream_t stream,
+                               bool pdl, int device) {
+    if (mma_n == 16) return launch_mp<16>(w_map, x_map, args, ctas, stream, pdl, device);
+    return launch_mp<32>(w_map, x_map, args, ctas, stream, pdl, device);
+}
+
+}  // namespace skinny

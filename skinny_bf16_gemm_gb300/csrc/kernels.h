@@ -1,0 +1,45 @@
+// Launch interface between the C ABI (api.cu) and the kernel translation units.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace skinny {
+
+// Bits of the device error word (one per waiting role that gave up).
+enum ErrorBits : int {
+    kErrProducerWait = 1,   // TMA producer: a pipeline slot never came free
+    kErrMmaFullWait = 2,    // MMA issuer: a stage's copies never landed
+    kErrMmaAccWait = 4,     // MMA issuer: the epilogue never released an accumulator
+    kErrEpilogueWait = 8,   // epilogue: an accumulator never completed
+    kErrDrain = 16,         // teardown: in-flight copies or MMAs did not finish
+    kErrSelftest = 32,      // the watchdog self-test's deliberate wait ran out
+};
+
+struct GemmArgs {
+    int M, N, K;
+    uint16_t *out;          // [M, N] BF16 patterns
+    float *partials;        // [2 * ctas][32][128] FP32 split-K partial tiles
+    unsigned *counters;     // [ctas] arrival counters, zero between calls
+    int *err;               // device error word
+    unsigned long long wait_limit_ns;
+    int selftest;           // 1: the MMA role waits on a barrier nothing completes
+};
+
+// Pipeline depth and shared memory of the decode GEMM for a padded row count.
+int gemm_stages(int mma_n);
+int gemm_smem_bytes(int mma_n);
+
+// Launch the decode GEMM: grid = ctas CTAs of 192 threads.
+cudaError_t launch_decode_gemm(const CUtensorMap &w_map, const CUtensorMap &x_map,
+                               const GemmArgs &args, int mma_n, int ctas, cudaStream_t stream,
+                               bool pdl, int device);
+
+// Launch reduce + residual + RMSNorm over rows of 7168: M clusters of
+// ctas_per_row CTAs.
+cudaError_t launch_reduce_rmsnorm(const void *partials, int TP, const void *residual,
+                                  const void *gamma, void *out, void *residual_out, int M,
+                                  float eps, int ctas_per_row, cudaStream_t stream, bool pdl);
+
+}  // namespace skinny

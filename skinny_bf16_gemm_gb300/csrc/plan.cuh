@@ -1,0 +1,87 @@
+// Work split of the decode GEMM (shared by the host planner and the kernel).
+//
+// The weight W[N, K] is cut into tiles of 128 rows (one MMA M extent) and each
+// tile's K range into blocks of 64 (one 128-byte swizzle row of BF16). The
+// tiles * kblocks weight blocks, in tile-major order, are dealt to G persistent
+// CTAs as contiguous ranges of (almost) equal length ("stream-K"): every CTA
+// streams the same number of weight bytes whatever N and K are, so no SM idles
+// in a partial last wave. A tile whose K range spans several CTAs is finished by
+// the last of them to arrive, which adds the others' FP32 partial sums in K order.
+#pragma once
+
+#include <cstdint>
+
+namespace skinny {
+
+constexpr int kBlockN = 128;       // weight rows per tile = MMA M
+constexpr int kBlockK = 64;        // K per pipeline stage: 128 bytes of BF16
+constexpr int kMaxM = 32;          // rows of x (MMA N is 16 or 32)
+constexpr int kSlotFloats = kMaxM * kBlockN;  // one FP32 partial tile [m][row]
+
+struct GemmGeometry {
+    int M, N, K;
+    int tiles;        // ceil(N / 128)
+    int kblocks;      // ceil(K / 64)
+    long long blocks; // tiles * kblocks
+    int ctas;         // G
+};
+
+__host__ __device__ inline GemmGeometry make_geometry(int M, int N, int K, int num_sms) {
+    GemmGeometry g;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.tiles = (N + kBlockN - 1) / kBlockN;
+    g.kblocks = (K + kBlockK - 1) / kBlockK;
+    g.blocks = static_cast<long long>(g.tiles) * g.kblocks;
+    g.ctas = static_cast<int>(g.blocks < num_sms ? g.blocks : num_sms);
+    return g;
+}
+
+// First weight block of CTA c (c = ctas gives the end of the last range).
+__host__ __device__ inline long long cta_begin(const GemmGeometry &g, int c) {
+    return (g.blocks * c) / g.ctas;
+}
+
+// The CTA whose range holds weight block i: the largest c with cta_begin(c) <= i.
+__host__ __device__ inline int block_owner(const GemmGeometry &g, long long i) {
+    return static_cast<int>(((i + 1) * g.ctas - 1) / g.blocks);
+}
+
+// Scratch slot of CTA c's partial sum for tile t: two per CTA, one for the tile
+// its range starts in and one for the tile it ends in.
+__host__ __device__ inline int partial_slot(const GemmGeometry &g, int c, int t) {
+    return 2 * c + (t == static_cast<int>(cta_begin(g, c) / g.kblocks) ? 0 : 1);
+}
+
+// Piece q of CTA c's range: tile t, blocks [kb0, kb1) of it.
+struct Piece {
+    int tile, kb0, kb1;
+};
+
+__host__ __device__ inline int cta_piece_count(const GemmGeometry &g, int c) {
+    long long b0 = cta_begin(g, c), b1 = cta_begin(g, c + 1);
+    if (b1 <= b0) return 0;
+    return static_cast<int>((b1 - 1) / g.kblocks - b0 / g.kblocks + 1);
+}
+
+__host__ __device__ inline Piece cta_piece(const GemmGeometry &g, int c, int q) {
+    long long b0 = cta_begin(g, c), b1 = cta_begin(g, c + 1);
+    int t = static_cast<int>(b0 / g.kblocks) + q;
+    long long t0 = static_cast<long long>(t) * g.kblocks;
+    Piece p;
+    p.tile = t;
+    p.kb0 = static_cast<int>((b0 > t0 ? b0 : t0) - t0);
+    p.kb1 = static_cast<int>((b1 < t0 + g.kblocks ? b1 : t0 + g.kblocks) - t0);
+    return p;
+}
+
+// CTAs contributing to tile t: [first, last].
+__host__ __device__ inline void tile_contributors(const GemmGeometry &g, int t, int &first,
+                                                  int &last) {
+    long long t0 = static_cast<long long>(t) * g.kblocks;
+    first = block_owner(g, t0);
+    last = block_owner(g, t0 + g.kblocks - 1);
+}
+
+}  // namespace skinny

@@ -1,0 +1,220 @@
+// Reduce + residual + RMSNorm over rows of 7168 BF16 values on GB300 (sm_103a)
+// ("drafter/comm": module text and ArNorm; "cutedsl/common/twoshot": reduce).
+//
+// Per element of row m, column c (bit-exact):
+//   s = p[0][m][c]; s = s + p[r][m][c] for r = 1..TP-1      (FP32, round to nearest)
+//   a = BF16(s);  h = residual ? BF16(a + residual[m][c]) : a  ->  residual_out
+// then per row: rstd = rsqrt(sum_c h^2 / 7168 + eps) (FP32) and
+//   out[m][c] = BF16((h * rstd) * gamma[c]).
+//
+// Layout: one cluster of C CTAs per row (grid C x M); CTA r of the cluster owns
+// the 896 / C 16-byte fragments (8 BF16 each) r*896/C .. ; thread t owns one
+// fragment, so a whole row's TP + 1 loads per thread are in flight at once. The
+// row's sum of squares: an FMA chain over the thread's 8 values, a warp butterfly,
+// the warps in order, then the C CTA sums exchanged through distributed shared
+// memory and added in CTA order (every CTA gets the same bits).
+// With programmatic dependent launch, gamma (a weight) is loaded before waiting
+// for the previous kernel; the partial rows and the residual after.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace skinny {
+namespace {
+
+constexpr int kHidden = 7168;
+constexpr int kRowFrags = kHidden / 8;  // 896 fragments of 16 bytes
+constexpr int kMaxTP = 8;
+
+template <int C>
+struct ReduceShape {
+    static constexpr int kFrags = kRowFrags / C;               // fragments per CTA
+    static constexpr int kThreads = (kFrags + 31) / 32 * 32;   // whole warps
+    static constexpr int kWarps = kThreads / 32;
+    static_assert(kRowFrags % C == 0, "row fragments must split evenly");
+};
+
+__device__ __forceinline__ float lo_bf16(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float hi_bf16(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint32_t bf16_bits(float v) {
+    return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v)));
+}
+
+__device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8]) {
+    f[0] = lo_bf16(v.x); f[1] = hi_bf16(v.x);
+    f[2] = lo_bf16(v.y); f[3] = hi_bf16(v.y);
+    f[4] = lo_bf16(v.z); f[5] = hi_bf16(v.z);
+    f[6] = lo_bf16(v.w); f[7] = hi_bf16(v.w);
+}
+
+__device__ __forceinline__ uint4 pack8(const uint32_t (&b)[8]) {
+    return make_uint4(b[0] | (b[1] << 16), b[2] | (b[3] << 16), b[4] | (b[5] << 16),
+                      b[6] | (b[7] << 16));
+}
+
+template <int C, bool RES>
+__global__ void __launch_bounds__(ReduceShape<C>::kThreads)
+    reduce_rmsnorm_kernel(const uint4 *__restrict__ partials, int TP, const uint4 *residual,
+                          const uint4 *__restrict__ gamma, uint4 *__restrict__ out,
+                          uint4 *residual_out, int M, float eps) {
+    using R = ReduceShape<C>;
+    __shared__ float warp_sums[R::kWarps];
+    __shared__ float parts[C];
+
+    const int tid = threadIdx.x;
+    const int rank = C > 1 ? static_cast<int>(blockIdx.x) : 0;  // cluster spans x
+    const int row = blockIdx.y;
+    const bool active = tid < R::kFrags;
+    const int frag = rank * R::kFrags + tid;
+    const size_t row_off = static_cast<size_t>(row) * kRowFrags + frag;
+
+    if constexpr (C > 1) {
+        // Peers' shared memory is written below; make sure every CTA has started.
+        asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+    }
+
+    uint4 gw = make_uint4(0, 0, 0, 0);
+    if (active) gw = __ldg(gamma + frag);
+    ptx::pdl_launch_dependents();
+    ptx::pdl_wait();  // the partial rows may be the previous kernel's output
+
+    float h[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float ss = 0.0f;
+    if (active) {
+        uint4 pv[kMaxTP];
+#pragma unroll
+        for (int r = 0; r < kMaxTP; ++r)
+            if (r < TP) pv[r] = __ldcs(partials + static_cast<size_t>(r) * M * kRowFrags + row_off);
+        uint4 rv = make_uint4(0, 0, 0, 0);
+        if constexpr (RES) rv = __ldcs(residual + row_off);
+
+        float s[8];
+        unpack8(pv[0], s);  // the sum starts from slot 0 (keeps -0)
+#pragma unroll
+        for (int r = 1; r < kMaxTP; ++r) {
+            if (r < TP) {
+                float t[8];
+                unpack8(pv[r], t);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) s[j] = __fadd_rn(s[j], t[j]);
+            }
+        }
+        uint32_t hb[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) hb[j] = bf16_bits(s[j]);
+        if constexpr (RES) {
+            float res[8];
+            unpack8(rv, res);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                hb[j] = bf16_bits(__fadd_rn(__uint_as_float(hb[j] << 16), res[j]));
+        }
+        residual_out[row_off] = pack8(hb);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            h[j] = __uint_as_float(hb[j] << 16);
+            ss = __fmaf_rn(h[j], h[j], ss);
+        }
+    }
+
+    // Row sum of squares: warp butterfly, warps in order, CTAs in order.
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xFFFFFFFFu, ss, o));
+    if ((tid & 31) == 0) warp_sums[tid >> 5] = ss;
+    __syncthreads();
+    if constexpr (C > 1) {
+        asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+        if (tid == 0) {
+            float block = warp_sums[0];
+#pragma unroll
+            for (int w = 1; w < R::kWarps; ++w) block = __fadd_rn(block, warp_sums[w]);
+            const uint32_t local = ptx::smem_addr(&parts[rank]);
+#pragma unroll
+            for (int peer = 0; peer < C; ++peer)
+                ptx::st_cluster_f32(ptx::map_to_cluster_rank(local, peer), block);
+        }
+        ptx::cluster_sync();
+    } else {
+        if (tid == 0) {
+            float block = warp_sums[0];
+            for (int w = 1; w < R::kWarps; ++w) block = __fadd_rn(block, warp_sums[w]);
+            parts[0] = block;
+        }
+        __syncthreads();
+    }
+    float total = parts[0];
+#pragma unroll
+    for (int c = 1; c < C; ++c) total = __fadd_rn(total, parts[c]);
+    const float rstd = rsqrtf(__fadd_rn(__fdiv_rn(total, static_cast<float>(kHidden)), eps));
+
+    if (active) {
+        float g[8];
+        unpack8(gw, g);
+        uint32_t ob[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) ob[j] = bf16_bits(__fmul_rn(__fmul_rn(h[j], rstd), g[j]));
+        out[row_off] = pack8(ob);
+    }
+}
+
+template <int C, bool RES>
+cudaError_t launch_c(const void *partials, int TP, const void *residual, const void *gamma,
+                     void *out, void *residual_out, int M, float eps, cudaStream_t stream,
+                     bool pdl) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(C, M, 1);
+    cfg.blockDim = dim3(ReduceShape<C>::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    if (C > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = C;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    if (pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, reduce_rmsnorm_kernel<C, RES>,
+                              static_cast<const uint4 *>(partials), TP,
+                              static_cast<const uint4 *>(residual),
+                              static_cast<const uint4 *>(gamma), static_cast<uint4 *>(out),
+                              static_cast<uint4 *>(residual_out), M, eps);
+}
+
+template <int C>
+cudaError_t launch_res(const void *partials, int TP, const void *residual, const void *gamma,
+                       void *out, void *residual_out, int M, float eps, cudaStream_t stream,
+                       bool pdl) {
+    if (residual)
+        return launch_c<C, true>(partials, TP, residual, gamma, out, residual_out, M, eps,
+                                 stream, pdl);
+    return launch_c<C, false>(partials, TP, residual, gamma, out, residual_out, M, eps, stream,
+                              pdl);
+}
+
+}  // namespace
+
+cudaError_t launch_reduce_rmsnorm(const void *partials, int TP, const void *residual,
+                                  const void *gamma, void *out, void *residual_out, int M,
+                                  float eps, int ctas_per_row, cudaStream_t stream, bool pdl) {
+    switch (ctas_per_row) {
+        case 1: return launch_res<1>(partials, TP, residual, gamma, out, residual_out, M, eps, stream, pdl);
+        case 2: return launch_res<2>(partials, TP, residual, gamma, out, residual_out, M, eps, stream, pdl);
+        case 4: return launch_res<4>(partials, TP, residual, gamma, out, residual_out, M, eps, stream, pdl);
+        case 8: return launch_res<8>(partials, TP, residual, gamma, out, residual_out, M, eps, stream, pdl);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace skinny

@@ -1,0 +1,199 @@
+"""The C ABI without a GPU: it builds, exports every declared symbol, rejects bad
+arguments before touching CUDA, and its decode-GEMM work split covers every
+weight block exactly once (the host planner shares its code with the kernel)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import skinny_bf16_gemm_gb300 as sk
+from skinny_bf16_gemm_gb300 import build as skbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "skinny.h")
+GOLDEN = os.path.join(ROOT, "tests", "golden", "pages_facts.txt")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    skbuild.build()
+    return sk.load_library()
+
+
+def declared_functions():
+    names = []
+    for line in open(HEADER):
+        m = re.match(r"^SKINNY_API\s+[\w\s\*]*?\b(\w+)\s*\(", line)
+        if m:
+            names.append(m.group(1))
+    return names
+
+
+def pages_facts():
+    facts = {}
+    for line in open(GOLDEN):
+        line = line.split("#", 1)[0].split()
+        if len(line) == 2:
+            facts[line[0]] = int(line[1], 0)
+    return facts
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert {"decode_gemm_bf16", "reduce_residual_rmsnorm", "skinny_status_string"} <= set(names)
+    for name in names:
+        assert hasattr(lib, name), f"{name} declared in skinny.h but not exported"
+
+
+def test_only_declared_symbols_are_exported(lib):
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", sk.LIBRARY], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
+    assert exported == set(declared_functions())
+
+
+def test_status_strings(lib):
+    for code in range(11):
+        assert sk.status_string(code) != "unknown status"
+    assert sk.status_string(999) == "unknown status"
+
+
+def test_header_constants_match_the_pages():
+    facts = pages_facts()
+    text = open(HEADER).read()
+    consts = dict(re.findall(r"#define (SKINNY_\w+) (\d+)", text))
+    assert int(consts["SKINNY_HIDDEN"]) == facts["hidden"] == sk.HIDDEN
+    assert int(consts["SKINNY_GEMM_MAX_M"]) == facts["warp_rows"] == sk.GEMM_MAX_M
+    assert int(consts["SKINNY_REDUCE_MAX_M"]) == facts["twoshot_cap"] == sk.REDUCE_MAX_M
+    # The ArNorm geometry the pages print: 8 CTAs x 112 fragments x 8 BF16 = 7168.
+    assert facts["ar_ctas"] * facts["ar_frags_per_cta"] * facts["fragment_bf16"] == facts["hidden"]
+    assert facts["ar_cols_per_cta"] == facts["ar_frags_per_cta"] * facts["fragment_bf16"]
+
+
+def _gate(n, k, facts):
+    """The pages' warp split-K shape gate (drafter/linears, warp_eligible)."""
+    if n % facts["gate_n_multiple"] or k % facts["gate_k_multiple"]:
+        return False
+    tiles = facts["gate_max_k_tiles"]
+    return k // 128 <= tiles or (k % 256 == 0 and k // 256 <= tiles)
+
+
+def test_accepted_shapes_cover_the_pages_gate(lib):
+    """Every (N, K) the pages' gate serves is accepted here (plus K = 18432 of the
+    layer chain, which the gate refuses); the gate's own example holds."""
+    facts = pages_facts()
+    assert facts["tp1_down_k"] // 256 == facts["tp1_down_k_tiles"]
+    assert _gate(7168, facts["tp1_down_k"], facts)
+    assert not _gate(7168, 18432, facts)
+    for n in (16, 2048, 4096, 7168, 12288, 18432, 20480):
+        for k in (128, 7168, 14336, 18432):
+            for m in (1, 32):
+                sk.gemm_plan(m, n, k, 152)
+
+
+@pytest.mark.parametrize("args,code", [
+    ((0, 16, 64), 2), ((33, 16, 64), 2), ((4, 0, 64), 2), ((4, 16, 0), 2), ((4, 16, 12), 2),
+])
+def test_gemm_rejects_shapes_before_cuda(lib, args, code):
+    M, N, K = args
+    buf = ctypes.create_string_buffer(1 << 16)
+    p = ctypes.addressof(buf) + (-ctypes.addressof(buf)) % 256
+    assert lib.decode_gemm_bf16(p, p + 8192, p + 16384, M, N, K, None) == code
+
+
+def test_gemm_rejects_null_alignment_alias_before_cuda(lib):
+    buf = ctypes.create_string_buffer(1 << 20)
+    p = ctypes.addressof(buf) + (-ctypes.addressof(buf)) % 256
+    assert lib.decode_gemm_bf16(None, p, p + 65536, 4, 16, 64, None) == 1
+    assert lib.decode_gemm_bf16(p, None, p + 65536, 4, 16, 64, None) == 1
+    assert lib.decode_gemm_bf16(p, p + 4096, None, 4, 16, 64, None) == 1
+    assert lib.decode_gemm_bf16(p + 8, p + 4096, p + 65536, 4, 16, 64, None) == 3
+    assert lib.decode_gemm_bf16(p, p + 4104, p + 65536, 4, 16, 64, None) == 3
+    assert lib.decode_gemm_bf16(p, p + 4096, p + 65537, 4, 16, 64, None) == 3
+    # out overlapping x, out overlapping W
+    assert lib.decode_gemm_bf16(p, p + 4096, p + 256, 4, 16, 64, None) == 6
+    assert lib.decode_gemm_bf16(p, p + 4096, p + 4096 + 512, 4, 16, 64, None) == 6
+
+
+def test_reduce_rejects_before_cuda(lib):
+    buf = ctypes.create_string_buffer(1 << 22)
+    p = ctypes.addressof(buf) + (-ctypes.addressof(buf)) % 256
+    row = 7168 * 2
+    part, res, gam, out, rout = p, p + 8 * row * 2, p + 10 * row * 2, p + 11 * row * 2, p + 13 * row * 2
+    f = lib.reduce_residual_rmsnorm
+    assert f(None, 8, res, gam, out, rout, 2, 1e-6, None) == 1
+    assert f(part, 8, res, None, out, rout, 2, 1e-6, None) == 1
+    assert f(part, 0, res, gam, out, rout, 2, 1e-6, None) == 2
+    assert f(part, 9, res, gam, out, rout, 2, 1e-6, None) == 2
+    assert f(part, 8, res, gam, out, rout, 0, 1e-6, None) == 2
+    assert f(part, 8, res, gam, out, rout, 65, 1e-6, None) == 2
+    assert f(part, 8, res, gam, out, rout, 2, 0.0, None) == 10
+    assert f(part, 8, res, gam, out, rout, 2, float("nan"), None) == 10
+    assert f(part, 8, res, gam, out, rout, 2, float("inf"), None) == 10
+    assert f(part + 2, 8, res, gam, out, rout, 2, 1e-6, None) == 3
+    assert f(part, 8, res, gam, out + 8, rout, 2, 1e-6, None) == 3
+    assert f(part, 8, res, gam, out, out, 2, 1e-6, None) == 6          # out == residual_out
+    assert f(part, 8, res, gam, part, rout, 2, 1e-6, None) == 6        # out over partials
+    assert f(part, 8, res, gam, out, res + 16, 2, 1e-6, None) == 6     # partial residual overlap
+
+
+def test_calls_without_a_device_report_device_error(lib):
+    """With valid arguments but no CUDA device the call fails cleanly."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a CUDA device is present")
+    buf = ctypes.create_string_buffer(1 << 20)
+    p = ctypes.addressof(buf) + (-ctypes.addressof(buf)) % 256
+    assert lib.decode_gemm_bf16(p, p + 4096, p + 65536, 4, 16, 64, None) == 4
+
+
+SHAPES = [(1, 16, 64, 152), (4, 2048, 7168, 152), (16, 18432, 7168, 152),
+          (16, 7168, 18432, 152), (32, 20480, 7168, 152), (3, 200, 136, 152),
+          (8, 128, 64, 152), (5, 12288, 7168, 148), (2, 4096, 7168, 7), (1, 1, 8, 152),
+          (32, 1000, 1000, 152), (7, 300, 4096, 64)]
+
+
+@pytest.mark.parametrize("M,N,K,sms", SHAPES)
+def test_work_split_covers_every_block_once(lib, M, N, K, sms):
+    plan = sk.gemm_plan(M, N, K, sms)
+    assert plan.tiles == -(-N // 128) and plan.kblocks == -(-K // 64)
+    assert plan.blocks == plan.tiles * plan.kblocks
+    assert plan.ctas == min(sms, plan.blocks)
+    assert plan.mma_n == (16 if M <= 16 else 32)
+    assert plan.smem_bytes <= 232448
+    seen = {}
+    per_cta = []
+    contributors = {}
+    slots = set()
+    for c in range(plan.ctas):
+        pieces = sk.gemm_cta_pieces(M, N, K, sms, c)
+        assert pieces, f"CTA {c} has no work"
+        n_blocks = 0
+        for (t, kb0, kb1, slot) in pieces:
+            assert 0 <= kb0 < kb1 <= plan.kblocks
+            for kb in range(kb0, kb1):
+                assert (t, kb) not in seen, f"block {(t, kb)} twice"
+                seen[(t, kb)] = c
+            n_blocks += kb1 - kb0
+            whole = kb0 == 0 and kb1 == plan.kblocks
+            assert (slot == -1) == whole
+            if not whole:
+                assert slot not in slots and 0 <= slot < 2 * plan.ctas
+                slots.add(slot)
+            contributors.setdefault(t, []).append(c)
+        per_cta.append(n_blocks)
+    assert len(seen) == plan.blocks
+    # Balanced: every CTA streams the same number of blocks, give or take one.
+    assert max(per_cta) - min(per_cta) <= 1
+    # Contributors of a tile are consecutive CTAs, in K order; the counter index
+    # (first contributor) is distinct for every shared tile.
+    firsts = []
+    for t, cs in contributors.items():
+        assert cs == list(range(cs[0], cs[0] + len(cs)))
+        order = [seen[(t, kb)] for kb in range(plan.kblocks)]
+        assert order == sorted(order)
+        if len(cs) > 1:
+            firsts.append(cs[0])
+    assert len(firsts) == len(set(firsts)) == plan.split_tiles

@@ -1,0 +1,151 @@
+"""GPU parity of decode_gemm_bf16 with the oracle, through the C ABI.
+
+Tolerance (oracle/compare.py): within 1 BF16 ulp of the binary64 result rounded
+to BF16 on >= 99.99 % of elements and within 2 on all, with ulps of outputs that
+cancel below 2^-11 * sum|x_k w_k| measured at that floor (FP32 accumulation noise
+makes a finer ulp meaningless there). Integer inputs must match bit for bit:
+every partial sum is exact in FP32, whatever the summation order."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import compare
+import skinny_bf16_gemm_gb300 as sk
+import workloads
+from gpu_helpers import (Guarded, check_gemm_full, check_gemm_sampled, gemm_inputs_device,
+                         sample_columns)
+
+pytestmark = pytest.mark.gpu
+
+
+def run_gemm(x, W):
+    M, N = x.shape[0], W.shape[0]
+    out = Guarded((M, N))
+    sk.decode_gemm_bf16(x, W, out.tensor)
+    torch.cuda.synchronize()
+    out.check()
+    st, word = sk.device_error()
+    assert st == 0 and word == 0, f"device error word {word}"
+    return out.tensor
+
+
+# Small shapes the oracle finishes in seconds: several 128-row tiles, ragged N and
+# K tails, every M class (MMA N = 16 and 32), tiles split across many CTAs.
+SMALL = [(1, 16, 64), (1, 1, 8), (2, 128, 8), (3, 200, 136), (4, 2048, 7168),
+         (5, 384, 1000), (8, 1000, 520), (16, 640, 7168), (17, 256, 4096),
+         (24, 130, 200), (31, 257, 72), (32, 384, 7168), (32, 2048, 1024)]
+
+
+@pytest.mark.parametrize("M,N,K", SMALL)
+def test_gemm_small_full_compare(cuda_ok, M, N, K):
+    x, W = gemm_inputs_device(M, N, K, workloads.seed_for("small", M, N, K))
+    out = run_gemm(x, W)
+    check_gemm_full(x, W, out)
+
+
+@pytest.mark.parametrize("M,N,K", [(32, 2048, 7168), (7, 1152, 18432), (1, 640, 7168)])
+def test_gemm_integer_inputs_bit_exact(cuda_ok, M, N, K):
+    """x, W in [-4, 4]: all partial sums are integers below 2^24, so any FP32
+    order is exact and the GPU must equal the oracle bit for bit. Pins the tile,
+    split-K and transpose wiring independently of rounding."""
+    x, W = gemm_inputs_device(M, N, K, workloads.seed_for("int", M, N, K), kind="int")
+    out = run_gemm(x, W)
+    check_gemm_full(x, W, out, exact_bits_required=True)
+
+
+def test_gemm_pr1(cuda_ok):
+    """PR1: M=4, N=2048, K=7168, x ~ N(0,1), W ~ N(0,1/K), seed 0 (full compare)."""
+    inp = workloads.gemm_inputs(4, 2048, 7168, 0)
+    x, W = inp.x.cuda(), inp.W.cuda()
+    out = run_gemm(x, W)
+    check_gemm_full(x, W, out)
+
+
+FULL_SIZE = ([(m, n, 7168) for m in (1, 2, 4, 8, 16, 24, 32) for n in (4096, 12288, 18432)]
+             + [(m, 20480, 7168) for m in (1, 8, 32)]
+             + [(16, 18432, 7168), (16, 7168, 18432)])
+
+
+@pytest.mark.parametrize("M,N,K", FULL_SIZE)
+def test_gemm_full_size_sampled(cuda_ok, M, N, K):
+    """The sweep, lm_head and chain shapes at full size, on sampled output columns
+    spread over every tile (the oracle computes them one by one)."""
+    x, W = gemm_inputs_device(M, N, K, workloads.seed_for("full", M, N, K))
+    out = run_gemm(x, W)
+    check_gemm_sampled(x, W, out, sample_columns(N, seed=M * 7 + N))
+
+
+def test_gemm_deterministic(cuda_ok):
+    x, W = gemm_inputs_device(8, 4096, 7168, 11)
+    a = run_gemm(x, W)
+    b = run_gemm(x, W)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_gemm_special_inputs(cuda_ok):
+    """W = [I | 0] reproduces x; negating W negates out; scaling W by 2 doubles out."""
+    M, N, K = 8, 512, 1024
+    x, _ = gemm_inputs_device(M, N, K, 21)
+    eye = torch.zeros(N, K, dtype=torch.bfloat16, device="cuda")
+    eye[torch.arange(N), torch.arange(N)] = 1
+    out = run_gemm(x, eye)
+    want = x[:, :N].clone()
+    want.view(torch.int16)[want.view(torch.int16) == -32768] = 0
+    assert torch.equal(out.view(torch.int16), want.view(torch.int16))
+    _, W = gemm_inputs_device(M, N, K, 22)
+    base = run_gemm(x, W)
+    neg = run_gemm(x, -W)
+    nz = base.view(torch.int16) & 0x7FFF != 0
+    assert torch.equal(neg[nz], -base[nz])
+    two = run_gemm(x, W * 2)
+    assert torch.equal(two.float(), base.float() * 2)
+
+
+def test_gemm_vs_cublas_informational(cuda_ok):
+    """torch.mm (cuBLAS) reaches the same results within the same tolerance;
+    the two differ only in summation order."""
+    x, W = gemm_inputs_device(16, 4096, 7168, 31)
+    ours = run_gemm(x, W)
+    ref = torch.mm(x, W.t())
+    d = compare.ulp_distance(workloads.bits(ours), workloads.bits(ref))
+    assert float((d <= 1).mean()) > 0.99
+
+
+def test_gemm_rejects_bad_device_args(cuda_ok):
+    lib = sk.load_library()
+    x = torch.zeros(4, 64, dtype=torch.bfloat16, device="cuda")
+    W = torch.zeros(16, 64, dtype=torch.bfloat16, device="cuda")
+    out = torch.zeros(4, 16, dtype=torch.bfloat16, device="cuda")
+    host = torch.zeros(4, 16, dtype=torch.bfloat16)
+    assert lib.decode_gemm_bf16(x.data_ptr(), W.data_ptr(), host.data_ptr(), 4, 16, 64, None) == 4
+    assert lib.decode_gemm_bf16(x.data_ptr() + 2, W.data_ptr(), out.data_ptr(), 4, 16, 64, None) == 3
+    assert lib.decode_gemm_bf16(x.data_ptr(), W.data_ptr(), out.data_ptr(), 4, 16, 60, None) == 2
+
+
+def test_gemm_in_cuda_graph(cuda_ok):
+    """After one eager call the GEMM can be captured and replayed in a CUDA graph."""
+    x, W = gemm_inputs_device(4, 2048, 7168, 41)
+    eager = run_gemm(x, W)
+    out = torch.empty_like(eager)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            sk.decode_gemm_bf16(x, W, out)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
+
+
+def test_gemm_with_pdl_matches(cuda_ok):
+    """Programmatic dependent launch changes when kernels start, not their bits."""
+    x, W = gemm_inputs_device(16, 4096, 7168, 51)
+    base = run_gemm(x, W)
+    prev = sk.set_pdl(True)
+    try:
+        outs = [run_gemm(x, W) for _ in range(3)]
+    finally:
+        sk.set_pdl(prev)
+    for o in outs:
+        assert torch.equal(o.view(torch.int16), base.view(torch.int16))
