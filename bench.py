@@ -48,6 +48,9 @@ def parse():
     ap.add_argument("--pdl", type=int, default=1, help="programmatic dependent launch")
     ap.add_argument("--graph", type=int, default=0, help="replay the step as a CUDA graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="per-config GB/s of every GEMM and reduce config instead of the chain")
+    ap.add_argument("--sweep-calls", type=int, default=200)
     return ap.parse_args()
 
 
@@ -246,6 +249,90 @@ def run_reference(args, rank, world, cfg):
     return 0
 
 
+# ---- per-config sweep ----------------------------------------------------------------
+
+def _l2_bytes():
+    try:
+        return int(torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size)
+    except Exception:
+        return 126 * 2 ** 20
+
+
+def _rotation(nbytes):
+    """Copies of a buffer so that the rotation spans at least 3x L2."""
+    return max(2, -(-3 * _l2_bytes() // max(nbytes, 1)))
+
+
+def _time_calls(fn, calls, copies, stream):
+    for i in range(min(copies, 8)):
+        fn(i % copies)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for i in range(calls):
+        fn(i % copies)
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / calls
+
+
+def run_sweep(args):
+    import __graft_entry__
+    __graft_entry__.build()
+    import skinny_bf16_gemm_gb300 as sk
+    sk.set_pdl(bool(args.pdl))
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    peak, peak_kind = measured_peaks()
+    results = []
+    gemms = ([("pr1", workloads.PR1_GEMM)] + [("sweep", g) for g in workloads.GEMM_SWEEP]
+             + [("lm_head", g) for g in workloads.LM_HEAD]
+             + [("chain", workloads.CHAIN.gemm1()), ("chain", workloads.CHAIN.gemm2())])
+    for label, g in gemms:
+        copies = _rotation(g.weight_bytes())
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(workloads.seed_for("sweep", g.M, g.N, g.K))
+        Ws = [(torch.randn(g.N, g.K, device=dev, generator=gen) / g.K ** 0.5).to(torch.bfloat16)
+              for _ in range(copies)]
+        x = torch.randn(g.M, g.K, device=dev, generator=gen).to(torch.bfloat16)
+        out = torch.empty(g.M, g.N, device=dev, dtype=torch.bfloat16)
+        ours = _time_calls(lambda i: sk.decode_gemm_bf16(x, Ws[i], out), args.sweep_calls,
+                           copies, stream)
+        cub = _time_calls(lambda i: torch.mm(x, Ws[i].t(), out=out), args.sweep_calls, copies,
+                          stream)
+        nb = g.algorithmic_bytes()
+        results.append({"kind": "decode_gemm", "set": label, "M": g.M, "N": g.N, "K": g.K,
+                        "us": ours * 1e3, "GBps": nb / (ours * 1e-3) / 1e9,
+                        "frac_measured": nb / (ours * 1e-3) / 1e9 / peak,
+                        "frac_nominal_8000": nb / (ours * 1e-3) / 1e9 / 8000.0,
+                        "cublas_us": cub * 1e3, "cublas_GBps": nb / (cub * 1e-3) / 1e9,
+                        "rotation_copies": copies})
+        del Ws
+        torch.cuda.empty_cache()
+    reduces = [("pr1", workloads.PR1_REDUCE)] + [("sweep", r) for r in workloads.REDUCE_SWEEP]
+    for label, r in reduces:
+        per = 2 * r.width * r.M * (r.TP + 1)
+        copies = _rotation(per)
+        parts = [torch.randn(r.TP, r.M, r.width, device=dev).to(torch.bfloat16)
+                 for _ in range(copies)]
+        ress = [torch.randn(r.M, r.width, device=dev).to(torch.bfloat16) if r.residual else None
+                for _ in range(copies)]
+        gamma = (1 + 0.1 * torch.randn(r.width, device=dev)).to(torch.bfloat16)
+        out = torch.empty(r.M, r.width, device=dev, dtype=torch.bfloat16)
+        rout = torch.empty_like(out)
+        t = _time_calls(lambda i: sk.reduce_residual_rmsnorm(parts[i], ress[i], gamma, out, rout),
+                        args.sweep_calls, copies, stream)
+        nb = r.algorithmic_bytes()
+        results.append({"kind": "reduce_rmsnorm", "set": label, "TP": r.TP, "M": r.M,
+                        "residual": r.residual, "us": t * 1e3, "GBps": nb / (t * 1e-3) / 1e9,
+                        "frac_measured": nb / (t * 1e-3) / 1e9 / peak, "rotation_copies": copies})
+        del parts, ress
+        torch.cuda.empty_cache()
+    print(json.dumps({"sweep": results, "peak_gbs": peak, "peak_source": peak_kind,
+                      "pdl": bool(args.pdl), "calls_per_config": args.sweep_calls}), flush=True)
+    return 0
+
+
 # ---- our arm ------------------------------------------------------------------------
 
 def main():
@@ -254,6 +341,8 @@ def main():
     cfg = workloads.CHAIN
     if args.impl == "reference":
         return run_reference(args, rank, world, cfg)
+    if args.sweep:
+        return run_sweep(args)
 
     import __graft_entry__
     if world > 1:
