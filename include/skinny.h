@@ -99,6 +99,35 @@ SKINNY_API int decode_gemm_bf16(const void *x, const void *W, void *out,
                      int M, int N, int K, void *stream);
 
 /*
+ * decode_gemm_bf16_noalloc -- decode_gemm_bf16 that allocates no device memory
+ *   The drafter pages have no counterpart to this entry point; it exists for
+ *   callers that cannot let a library call cudaMalloc. Examples: code that runs
+ *   while a CUDA graph is being captured in the strict capture mode (there
+ *   cudaMalloc is an error that also invalidates the capture); serving engines
+ *   that give all spare device memory to their own pool at start-up, so any later
+ *   allocation fails or evicts cache; plug-ins that may only use their host
+ *   framework's allocator; latency-critical loops that cannot afford cudaMalloc's
+ *   implicit synchronisation.
+ *
+ *   Same arguments, layouts, results and errors as decode_gemm_bf16 (the same
+ *   kernel runs). The split-K scratch -- partial tiles, tile counters, error
+ *   word -- lives instead in one static device array of the library, 5.2 MB,
+ *   which every GPU that loads the library holds until the process exits. It has
+ *   partial-tile slots for 160 CTAs of up to 32 rows: the call runs with
+ *   min(SM count, 160) CTAs and rejects M > 32 with SKINNY_ERR_SHAPE.
+ *   The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   Each call first clears the counters and the error word with a
+ *   cudaMemsetAsync on `stream`, then launches the kernel. All calls share the
+ *   one array: calls whose GPU work may overlap (streams not ordered with each
+ *   other on the same device) race and give wrong results; order them. A kernel
+ *   wait that runs out still ends the kernel, but this entry point does not
+ *   report it (the next call clears the word); the output is then unspecified.
+ */
+SKINNY_API int decode_gemm_bf16_noalloc(const void *x, const void *W, void *out,
+                                        int M, int N, int K, void *stream);
+
+/*
  * reduce_residual_rmsnorm -- the ArNorm row operation on TP local slots
  *   ("drafter/comm": module text -- "summed in FP32 in rank order 0 .. TP-1 and
  *    rounded once to BF16 ..., the residual is added (one BF16 rounding) and the

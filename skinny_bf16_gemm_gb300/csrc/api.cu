@@ -212,6 +212,67 @@ int gemm_launch(const void *x, const void *W, void *out, int M, int N, int K, vo
     return SKINNY_OK;
 }
 
+// decode_gemm_bf16 with its split-K scratch in the static device array of
+// decode_gemm.cu: no device memory is allocated on this path.
+int gemm_launch_static(const void *x, const void *W, void *out, int M, int N, int K,
+                       void *stream) {
+    if (!x || !W || !out) return SKINNY_ERR_NULL;
+    int st = gemm_shape_ok(M, N, K);  // M <= 32 is also the static slots' row limit
+    if (st) return st;
+    if (!aligned(x, 16) || !aligned(W, 16) || !aligned(out, 2)) return SKINNY_ERR_ALIGN;
+    const size_t xb = static_cast<size_t>(M) * K * 2, wb = static_cast<size_t>(N) * K * 2,
+                 ob = static_cast<size_t>(M) * N * 2;
+    if (overlaps(out, ob, x, xb) || overlaps(out, ob, W, wb)) return SKINNY_ERR_ALIAS;
+    int dev;
+    if ((st = current_device(&dev))) return st;
+    DeviceState *d = nullptr;
+    if ((st = device_state(dev, &d))) return st;
+    if ((st = check_device_pointer(x, dev)) || (st = check_device_pointer(W, dev)) ||
+        (st = check_device_pointer(out, dev)))
+        return st;
+    StaticScratch sc;
+    if (static_scratch_for_current_device(&sc) != cudaSuccess) {
+        cudaGetLastError();
+        return SKINNY_ERR_DEVICE;
+    }
+    EncodeTiledFn enc;
+    if ((st = encoder(&enc))) return st;
+    const int mma_n = mma_n_for(M);
+    alignas(64) CUtensorMap w_map, x_map;
+    if ((st = encode_2d(enc, &w_map, W, N, K, kBlockN))) return st;
+    if ((st = encode_2d(enc, &x_map, x, M, K, mma_n))) return st;
+    // At most as many CTAs as the array has partial-tile slots for.
+    const GemmGeometry g = make_geometry(M, N, K, d->sms < sc.max_ctas ? d->sms : sc.max_ctas);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // The array keeps the previous call's contents: the tile counters and the
+    // error word must start this call at zero.
+    if (cudaMemsetAsync(sc.counters, 0, sc.zero_bytes, s) != cudaSuccess) {
+        cudaGetLastError();
+        return SKINNY_ERR_LAUNCH;
+    }
+    GemmArgs a;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.out = static_cast<uint16_t *>(out);
+    a.partials = sc.partials;
+    a.counters = sc.counters;
+    a.err = sc.err;
+    a.wait_limit_ns = kWaitLimitNs;
+    a.selftest = 0;
+    bool pdl;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        pdl = g_pdl;
+    }
+    cudaError_t e = launch_decode_gemm(w_map, x_map, a, mma_n, g.ctas, s, pdl, dev);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return SKINNY_ERR_LAUNCH;
+    }
+    return SKINNY_OK;
+}
+
 // CTAs per row of the reduce: enough rows x CTAs to spread a small problem over
 // many SMs, fewer (bigger) CTAs once rows alone fill the GPU.
 int reduce_ctas_per_row(int M) { return M <= 32 ? 8 : 4; }
@@ -225,6 +286,11 @@ extern "C" {
 
 int decode_gemm_bf16(const void *x, const void *W, void *out, int M, int N, int K, void *stream) {
     return gemm_launch(x, W, out, M, N, K, stream, 0, kWaitLimitNs);
+}
+
+int decode_gemm_bf16_noalloc(const void *x, const void *W, void *out, int M, int N, int K,
+                             void *stream) {
+    return gemm_launch_static(x, W, out, M, N, K, stream);
 }
 
 int skinny_watchdog_selftest(const void *x, const void *W, void *out, int M, int N, int K,

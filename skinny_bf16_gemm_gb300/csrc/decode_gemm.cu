@@ -26,6 +26,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "kernels.h"
 #include "plan.cuh"
 #include "ptx.cuh"
@@ -415,6 +417,55 @@ cudaError_t launch_decode_gemm(const CUtensorMap &w_map, const CUtensorMap &x_ma
                                bool pdl, int device) {
     if (mma_n == 16) return launch_mp<16>(w_map, x_map, args, ctas, stream, pdl, device);
     return launch_mp<32>(w_map, x_map, args, ctas, stream, pdl, device);
+}
+
+}  // namespace skinny
+
+// ---- scratch in a static device array (for decode_gemm_bf16_noalloc) -----------------
+//
+// The same kernel can run with its split-K scratch in this file-scope array
+// instead of memory from cudaMalloc. Sized for kStaticScratchCtas CTAs with
+// partial tiles of up to 32 rows: 2 slots per CTA, then one counter per CTA, then
+// the error word. Every GPU that loads the library holds it until the process
+// exits.
+namespace skinny {
+namespace {
+
+constexpr size_t kStaticPartialBytes =
+    static_cast<size_t>(2) * kStaticScratchCtas * kSlotFloats * sizeof(float);
+constexpr size_t kStaticCounterBytes = 1024;  // >= kStaticScratchCtas counters, 256-aligned
+constexpr size_t kStaticScratchBytes = kStaticPartialBytes + kStaticCounterBytes + 256;
+static_assert(kStaticScratchCtas * sizeof(unsigned) <= kStaticCounterBytes, "counter space");
+
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+std::mutex g_static_mutex;
+void *g_static_base[64] = {};
+
+}  // namespace
+
+cudaError_t static_scratch_for_current_device(StaticScratch *out) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_static_mutex);
+    if (g_static_base[dev] == nullptr) {
+        // Host code sees g_static_scratch only as a stand-in symbol; the array's
+        // device address has to be looked up, once per device, with it current.
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_static_scratch);
+        if (e != cudaSuccess) return e;
+        if (p == nullptr) return cudaErrorInvalidSymbol;
+        g_static_base[dev] = p;
+    }
+    char *base = static_cast<char *>(g_static_base[dev]);
+    out->partials = reinterpret_cast<float *>(base);
+    out->counters = reinterpret_cast<unsigned *>(base + kStaticPartialBytes);
+    out->err = reinterpret_cast<int *>(base + kStaticPartialBytes + kStaticCounterBytes);
+    out->zero_bytes = kStaticCounterBytes + sizeof(int);  // counters and error word
+    out->max_ctas = kStaticScratchCtas;
+    return cudaSuccess;
 }
 
 }  // namespace skinny

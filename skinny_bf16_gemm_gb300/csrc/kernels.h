@@ -36,6 +36,21 @@ cudaError_t launch_decode_gemm(const CUtensorMap &w_map, const CUtensorMap &x_ma
                                const GemmArgs &args, int mma_n, int ctas, cudaStream_t stream,
                                bool pdl, int device);
 
+// Split-K scratch held in a static device array (decode_gemm_bf16_noalloc).
+constexpr int kStaticScratchCtas = 160;   // CTAs the array holds partial tiles for
+
+struct StaticScratch {
+    float *partials;      // [2 * max_ctas][32][128] FP32
+    unsigned *counters;   // [max_ctas], contiguous with err
+    int *err;             // error word, right after the counter space
+    size_t zero_bytes;    // bytes from `counters` through `err` that must start at zero
+    int max_ctas;
+};
+
+// Device addresses of the static scratch on the current device; the first call
+// per device looks them up (cudaGetSymbolAddress).
+cudaError_t static_scratch_for_current_device(StaticScratch *out);
+
 // Launch reduce + residual + RMSNorm over rows of 7168: M clusters of
 // ctas_per_row CTAs.
 cudaError_t launch_reduce_rmsnorm(const void *partials, int TP, const void *residual,
