@@ -415,8 +415,13 @@ int skinny_gemm_plan_query(int M, int N, int K, int num_sms, skinny_gemm_plan *p
     plan->blocks = g.blocks;
     plan->ctas = g.ctas;
     plan->mma_n = mma_n_for(M);
-    plan->stages = gemm_stages(plan->mma_n);
-    plan->smem_bytes = gemm_smem_bytes(plan->mma_n);
+    bool pdl;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        pdl = g_pdl;
+    }
+    plan->stages = gemm_stages(plan->mma_n, pdl);
+    plan->smem_bytes = gemm_smem_bytes(plan->mma_n, pdl);
     int split = 0;
     for (int t = 0; t < g.tiles; ++t) {
         int first, last;

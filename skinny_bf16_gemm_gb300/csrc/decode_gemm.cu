@@ -41,13 +41,18 @@ constexpr int kTmemCols = 64;          // two accumulator buffers of 32 columns
 constexpr int kWBytes = kBlockN * kBlockK * 2;
 constexpr uint64_t kDrainLimitNs = 200000000ull;  // 0.2 s for copies already issued
 
-template <int MP>
+// MP: padded row count (MMA N). STAGES: shared-memory ring depth. The deep ring
+// (~185 KB) keeps the most bytes in flight; the shallow one (~92-101 KB) lets the
+// next kernel's CTAs be resident on the same SM while this one finishes, so
+// with programmatic dependent launch they stream weights across the boundary.
+template <int MP, int STAGES>
 struct Layout {
-    static constexpr int kStages = MP == 16 ? 10 : 9;
+    static constexpr int kStages = STAGES;
     static constexpr int kXBytes = MP * kBlockK * 2;
     static constexpr int kStageBytes = kWBytes + kXBytes;
     static constexpr int kBarOffset = kStages * kStageBytes;
-    static constexpr int kNumBars = 2 * kStages + 6;
+    static constexpr int kNumBars = 2 * kStages + 7;
+    static constexpr int kRingBytes = kStages * kStageBytes;
     static constexpr int kMiscOffset = kBarOffset + kNumBars * 8;
     static constexpr int kBytes = kMiscOffset + 16;
     static constexpr int kDynamicBytes = kBytes + 1024;  // slack to align the base to 1024
@@ -95,11 +100,11 @@ __device__ __forceinline__ uint16_t to_bf16_bits(float v) {
     return __bfloat16_as_ushort(__float2bfloat16_rn(v));
 }
 
-template <int MP>
+template <int MP, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_gemm_kernel(const __grid_constant__ CUtensorMap w_map,
                        const __grid_constant__ CUtensorMap x_map, const GemmArgs args) {
-    using L = Layout<MP>;
+    using L = Layout<MP, STAGES>;
     constexpr int S = L::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -111,6 +116,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t bar_acc_empty = bar_acc_full + 16;  // + 8 b
     const uint32_t bar_drain = bar_acc_empty + 16;
     const uint32_t bar_never = bar_drain + 8;
+    const uint32_t bar_fix = bar_never + 8;             // split-K fix-up bulk copies
     volatile uint32_t *misc = reinterpret_cast<volatile uint32_t *>(smem + L::kMiscOffset);
     // misc[0]: tensor-memory base, misc[1]: abort flag, misc[2]: "last to arrive" flag
 
@@ -131,6 +137,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::mbar_init(bar_drain, 1);
         ptx::mbar_init(bar_never, 1);
+        ptx::mbar_init(bar_fix, 1);
         misc[1] = 0u;
         misc[2] = 0u;
         ptx::fence_barrier_init();
@@ -267,6 +274,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quarter = warp & 3;              // TMEM lanes 32*quarter .. +31
         const int row = quarter * 32 + lane;       // weight row within the tile
         const int etid = threadIdx.x - 64;
+        // Tiles this CTA arrived last at: tile, first and last contributor, packed
+        // (register-resident; at most two).
+        int4 fin[2] = {make_int4(0, 0, 0, 0), make_int4(0, 0, 0, 0)};
+        int fin_count = 0;
+        bool fix_pending = false;
         for (int q = 0; q < pieces; ++q) {
             const Piece p = cta_piece(g, cta, q);
             const int b = q & 1;
@@ -304,14 +316,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 continue;
             }
-            // Shared tile: publish this CTA's partial, count arrivals; the last
-            // arrival adds every partial in K (= CTA) order and stores.
+            // Shared tile: publish this CTA's partial and count the arrival. The
+            // CTA that arrives last finishes the tile, but only after its own
+            // pieces are done (the shared-memory ring is free then).
             int first, last;
             tile_contributors(g, p.tile, first, last);
             float *mine = args.partials + static_cast<size_t>(partial_slot(g, cta, p.tile)) * kSlotFloats;
 #pragma unroll
             for (int m = 0; m < MP; ++m)
                 if (m < g.M) __stcg(mine + m * kBlockN + row, acc[m]);
+            ptx::fence_proxy_async_global();  // the finishing CTA reads it with bulk copies
             __threadfence();
             ptx::named_barrier_sync(1, kEpilogueThreads);
             if (etid == 0) {
@@ -322,25 +336,81 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ptx::named_barrier_sync(1, kEpilogueThreads);
             if (misc[2] != 0u) {
-                __threadfence();
-                if (in_range) {
+                // Only a range's first and last pieces can be partial.
+                const int4 rec = make_int4(p.tile, first, last, 0);
+                if (fin_count == 0) fin[0] = rec;
+                else fin[1] = rec;
+                fin_count = fin_count < 2 ? fin_count + 1 : 2;
+            }
+            ptx::named_barrier_sync(1, kEpilogueThreads);  // misc[2] is reused next piece
+        }
+
+        // Finish the shared tiles this CTA arrived last at (at most two: only a
+        // range's first and last pieces can be partial). Every partial, this
+        // CTA's own included, is pulled into the free ring with bulk copies --
+        // all in flight at once -- and added in K (= CTA) order.
+        if (!epilogue_any(*abort_flag != 0u)) {
+            const int slot_bytes = g.M * kBlockN * static_cast<int>(sizeof(float));
+            const int cap = L::kRingBytes / slot_bytes;
+            const float *staging = reinterpret_cast<const float *>(smem);
+            uint32_t fix_phase = 0;
+            bool failed = false;
+            for (int f = 0; f < fin_count && !failed; ++f) {
+                const int4 rec = f == 0 ? fin[0] : fin[1];
+                const int t = rec.x, first = rec.y, last = rec.z;
+                float sum[MP];
 #pragma unroll
-                    for (int m = 0; m < MP; ++m) {
-                        if (m >= g.M) continue;
-                        float sum = 0.0f;
-                        for (int c = first; c <= last; ++c) {
-                            const float v = c == cta
-                                                ? acc[m]
-                                                : __ldcg(args.partials +
-                                                         static_cast<size_t>(partial_slot(g, c, p.tile)) * kSlotFloats +
-                                                         m * kBlockN + row);
-                            sum = c == first ? v : __fadd_rn(sum, v);
+                for (int m = 0; m < MP; ++m) sum[m] = 0.0f;
+                for (int c0 = first; c0 <= last; c0 += cap) {
+                    const int c1 = last + 1 < c0 + cap ? last + 1 : c0 + cap;
+                    if (etid == 0) {
+                        __threadfence();
+                        ptx::fence_proxy_async_global();
+                        ptx::mbar_arrive_expect_tx(bar_fix, static_cast<uint32_t>((c1 - c0) * slot_bytes));
+                        for (int c = c0; c < c1; ++c)
+                            ptx::bulk_load(sbase + (c - c0) * slot_bytes,
+                                           args.partials + static_cast<size_t>(partial_slot(g, c, t)) * kSlotFloats,
+                                           slot_bytes, bar_fix);
+                    }
+                    fix_pending = true;
+                    const int r = bounded_wait(bar_fix, fix_phase, abort_flag, limit);
+                    if (r == kWaitTimeout) raise_error(args.err, abort_flag, kErrEpilogueWait);
+                    if (epilogue_any(r != kWaitDone)) {
+                        failed = true;
+                        break;
+                    }
+                    fix_pending = false;
+                    fix_phase ^= 1u;
+                    for (int c = c0; c < c1; ++c) {
+                        const float *src = staging + static_cast<size_t>(c - c0) * g.M * kBlockN + row;
+#pragma unroll
+                        for (int m = 0; m < MP; ++m) {
+                            if (m < g.M) {
+                                const float v = src[m * kBlockN];
+                                sum[m] = c == first ? v : __fadd_rn(sum[m], v);
+                            }
                         }
-                        args.out[static_cast<size_t>(m) * g.N + n] = to_bf16_bits(sum);
+                    }
+                    ptx::named_barrier_sync(1, kEpilogueThreads);  // staging is refilled next
+                }
+                if (failed) break;
+                const int n = t * kBlockN + row;
+                if (n < g.N) {
+#pragma unroll
+                    for (int m = 0; m < MP; ++m)
+                        if (m < g.M) args.out[static_cast<size_t>(m) * g.N + n] = to_bf16_bits(sum[m]);
+                }
+            }
+            if (fix_pending) {
+                // Copies still in flight must land before the CTA's memory is released.
+                const uint64_t t0 = ptx::global_timer_ns();
+                while (!ptx::mbar_try_wait(bar_fix, fix_phase)) {
+                    if (ptx::global_timer_ns() - t0 > kDrainLimitNs) {
+                        atomicOr(args.err, kErrDrain);
+                        break;
                     }
                 }
             }
-            ptx::named_barrier_sync(1, kEpilogueThreads);  // misc[2] is reused next piece
         }
     }
 
@@ -379,44 +449,59 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int MP>
-cudaError_t launch_mp(const CUtensorMap &w_map, const CUtensorMap &x_map, const GemmArgs &args,
-                      int ctas, cudaStream_t stream, bool pdl, int device) {
+template <int MP, int STAGES>
+cudaError_t launch_variant(const CUtensorMap &w_map, const CUtensorMap &x_map,
+                           const GemmArgs &args, int ctas, cudaStream_t stream, bool pdl,
+                           int device) {
+    using L = Layout<MP, STAGES>;
     static bool configured[64] = {};
     if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
     if (!configured[device]) {
-        cudaError_t e = cudaFuncSetAttribute(decode_gemm_kernel<MP>,
+        cudaError_t e = cudaFuncSetAttribute(decode_gemm_kernel<MP, STAGES>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             Layout<MP>::kDynamicBytes);
+                                             L::kDynamicBytes);
         if (e != cudaSuccess) return e;
         configured[device] = true;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(ctas, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = Layout<MP>::kDynamicBytes;
+    cfg.dynamicSmemBytes = L::kDynamicBytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, decode_gemm_kernel<MP>, w_map, x_map, args);
+    return cudaLaunchKernelEx(&cfg, decode_gemm_kernel<MP, STAGES>, w_map, x_map, args);
 }
+
+constexpr int kDeepStages16 = 10, kDeepStages32 = 9, kShallowStages = 5;
 
 }  // namespace
 
-int gemm_stages(int mma_n) { return mma_n == 16 ? Layout<16>::kStages : Layout<32>::kStages; }
+// The shallow ring goes with programmatic dependent launch (consecutive kernels
+// overlap on each SM); the deep ring otherwise.
+int gemm_stages(int mma_n, bool pdl) {
+    if (pdl) return kShallowStages;
+    return mma_n == 16 ? kDeepStages16 : kDeepStages32;
+}
 
-int gemm_smem_bytes(int mma_n) {
-    return mma_n == 16 ? Layout<16>::kDynamicBytes : Layout<32>::kDynamicBytes;
+int gemm_smem_bytes(int mma_n, bool pdl) {
+    if (mma_n == 16)
+        return pdl ? Layout<16, kShallowStages>::kDynamicBytes : Layout<16, kDeepStages16>::kDynamicBytes;
+    return pdl ? Layout<32, kShallowStages>::kDynamicBytes : Layout<32, kDeepStages32>::kDynamicBytes;
 }
 
 cudaError_t launch_decode_gemm(const CUtensorMap &w_map, const CUtensorMap &x_map,
                                const GemmArgs &args, int mma_n, int ctas, cudaStream_t stream,
                                bool pdl, int device) {
-    if (mma_n == 16) return launch_mp<16>(w_map, x_map, args, ctas, stream, pdl, device);
-    return launch_mp<32>(w_map, x_map, args, ctas, stream, pdl, device);
+    if (mma_n == 16) {
+        if (pdl) return launch_variant<16, kShallowStages>(w_map, x_map, args, ctas, stream, pdl, device);
+        return launch_variant<16, kDeepStages16>(w_map, x_map, args, ctas, stream, pdl, device);
+    }
+    if (pdl) return launch_variant<32, kShallowStages>(w_map, x_map, args, ctas, stream, pdl, device);
+    return launch_variant<32, kDeepStages32>(w_map, x_map, args, ctas, stream, pdl, device);
 }
 
 }  // namespace skinny

@@ -27,9 +27,10 @@ struct GemmArgs {
     int selftest;           // 1: the MMA role waits on a barrier nothing completes
 };
 
-// Pipeline depth and shared memory of the decode GEMM for a padded row count.
-int gemm_stages(int mma_n);
-int gemm_smem_bytes(int mma_n);
+// Pipeline depth and shared memory of the decode GEMM for a padded row count,
+// with or without programmatic dependent launch.
+int gemm_stages(int mma_n, bool pdl);
+int gemm_smem_bytes(int mma_n, bool pdl);
 
 // Launch the decode GEMM: grid = ctas CTAs of 192 threads.
 cudaError_t launch_decode_gemm(const CUtensorMap &w_map, const CUtensorMap &x_map,

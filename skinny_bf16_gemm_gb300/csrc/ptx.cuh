@@ -82,6 +82,22 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// Non-tensor bulk copy global -> this CTA's shared memory (16-byte aligned
+// addresses, size a multiple of 16), completion counted in bytes on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
+                                          uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// Order this thread's generic-proxy global accesses with async-proxy (bulk copy)
+// accesses that follow.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // ---- tcgen05 ------------------------------------------------------------------------
 
 // Allocate `ncols` tensor-memory columns (a power of two >= 32); the base address
