@@ -57,10 +57,8 @@ def parse():
 
 
 def dist_info():
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    return rank, world, local
+    from skinny_bf16_gemm_gb300.replicas import rank_info
+    return rank_info()
 
 
 def workload_config(cfg, extra=None):
@@ -405,7 +403,8 @@ def main():
     from skinny_bf16_gemm_gb300.chain import LayerChain
 
     device = torch.device("cuda", local)
-    inp = workloads.chain_inputs(cfg, workloads.seed_for("chain", rank), device=device)
+    from skinny_bf16_gemm_gb300.replicas import replica_seed
+    inp = workloads.chain_inputs(cfg, replica_seed(workloads.seed_for("chain"), rank), device=device)
     chain = LayerChain(inp.W1, inp.W2, inp.peers, inp.gamma, cfg.M, cfg.eps, device=device)
     chain.x.copy_(inp.x0)
     chain.res_in.copy_(inp.residual0)
@@ -447,14 +446,10 @@ def main():
     torch.cuda.synchronize()
     barrier()
     clock_info = clocks.stop()
-    ms = e0.elapsed_time(e1)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    from skinny_bf16_gemm_gb300 import replicas
+    ms = replicas.slowest_ms(e0.elapsed_time(e1), device=device)
     ms_per_step = ms / args.steps
-    value = world * cfg.step_bytes() / (ms_per_step * 1e-3) / 1e9
+    value = replicas.aggregate_throughput(cfg.step_bytes(), args.steps, ms, world)
     st, word = sk.device_error(local)
     if st != 0:
         raise RuntimeError(f"device error word {word} in the timed region")

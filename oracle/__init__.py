@@ -20,6 +20,8 @@ What each function follows (the vLLM DSpark drafter pages):
 * ``rmsnorm`` -- "drafter/comm" module text ("FP32 sum of squares, rsqrt(sum /
   7168 + eps), x * rstd * w rounded once") and ``ArNorm.kernel``'s last block.
   Evaluated in binary64 and rounded once.
+* ``gather_shards`` -- "drafter/comm", ``Gather`` docstring and module text:
+  every rank's [M, S] shard at columns r*S.. of the [M, TP*S] row; a byte move.
 * ``rmsnorm_f32_steps`` -- diagnostic: the same formula in the binary32 steps the
   kernel lists; never a parity reference.
 """
@@ -64,6 +66,8 @@ def _load():
             fn = getattr(lib, name)
             fn.argtypes = [u16p, u16p, u16p, ctypes.c_int, ctypes.c_int, ctypes.c_float]
             fn.restype = None
+        lib.oracle_gather_shards.argtypes = [u16p, ctypes.c_int, ctypes.c_int, ctypes.c_int, u16p]
+        lib.oracle_gather_shards.restype = None
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = ctypes.c_int
         _lib = lib
@@ -183,6 +187,15 @@ def reduce_residual_rmsnorm(partials, residual, gamma, eps):
     """(out, residual_out): the whole row op -- reduce, residual, then RMSNorm."""
     h = reduce_residual(partials, residual)
     return rmsnorm(h, gamma, eps), h
+
+
+def gather_shards(shards):
+    """[M, TP * S] rows from [TP, M, S] shards, rank r at columns r*S.."""
+    sh = _u16(shards)
+    TP, M, S = sh.shape
+    out = np.empty((M, TP * S), dtype=np.uint16)
+    _load().oracle_gather_shards(_ptr(sh), TP, M, S, _ptr(out))
+    return out
 
 
 def max_threads() -> int:

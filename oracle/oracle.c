@@ -261,6 +261,25 @@ void oracle_rmsnorm_f32_steps(const uint16_t *h, const uint16_t *gamma, uint16_t
     }
 }
 
+/* ---- gather ------------------------------------------------------------------ */
+
+/*
+ * out[m][r * S + j] = shards[r][m][j]: every rank's [M, S] shard placed at
+ * columns r*S .. r*S + S - 1 of the gathered [M, TP * S] rows ("drafter/comm",
+ * Gather docstring and module text: "rank r's at columns r S .."; gather_context
+ * and gather_logits build [M, TP * S] from [M, S] shards). A byte move: the
+ * values are copied unchanged (no sentinel cleaning -- the local slots have no
+ * sentinel). shards is [TP, M, S], out is [M, TP * S].
+ */
+void oracle_gather_shards(const uint16_t *shards, int TP, int M, int S, uint16_t *out)
+{
+    for (int r = 0; r < TP; ++r)
+        for (int m = 0; m < M; ++m)
+            for (int j = 0; j < S; ++j)
+                out[(size_t)m * (size_t)TP * (size_t)S + (size_t)r * (size_t)S + (size_t)j] =
+                    shards[((size_t)r * (size_t)M + (size_t)m) * (size_t)S + (size_t)j];
+}
+
 /* Threads OpenMP would use for the GEMM loop (reported beside CPU timings). */
 int oracle_max_threads(void)
 {

@@ -33,12 +33,13 @@ class Impl:
     decode_gemm: Callable          # (x_bits, W_bits) -> out_bits
     reduce_residual: Callable      # (partials_bits, residual_bits|None) -> bits
     rmsnorm: Callable              # (h_bits, gamma_bits, eps) -> bits
+    gather_shards: Callable = None  # (shards_bits [TP, M, S]) -> bits [M, TP*S]
 
 
 def oracle_impl():
     import oracle
     return Impl(oracle.bf16_from_f64_array, oracle.decode_gemm, oracle.reduce_residual,
-                oracle.rmsnorm)
+                oracle.rmsnorm, oracle.gather_shards)
 
 
 # ---- helpers -----------------------------------------------------------------
@@ -387,6 +388,43 @@ def pin_rmsnorm_invariants(impl: Impl, seed=9):
     return None
 
 
+# ---- gather ---------------------------------------------------------------------------
+
+def pin_gather_placement(impl: Impl, seed=12):
+    """Every element of the gathered row names where it came from: with shard
+    values encoding (rank, row, column), out[m][c] must be rank c // S, row m,
+    column c % S -- the pages' "rank r's at columns r S ..". Sentinel-like words
+    (+0, -0) pass through unchanged."""
+    TP, M, S = 4, 3, 24
+    r, m, j = np.meshgrid(np.arange(TP), np.arange(M), np.arange(S), indexing="ij")
+    code = (r * 64 + m * 16 + (j % 16)).astype(np.float32)  # small integers: exact in BF16
+    code[:, :, 16:] += 0.5 * (j[:, :, 16:] // 16)  # keep columns >= 16 distinct
+    shards = f32_to_bf16_torch(code)
+    shards[1, 2, 5] = 0x8000   # the -0 half of the sentinel pair stays
+    shards[1, 2, 4] = 0x0000
+    got = impl.gather_shards(shards)
+    if got.shape != (M, TP * S):
+        return f"shape {got.shape}"
+    for mm in range(M):
+        for c in range(TP * S):
+            if int(got[mm, c]) != int(shards[c // S, mm, c % S]):
+                return f"out[{mm}][{c}] is not shard[{c // S}][{mm}][{c % S}]"
+    return None
+
+
+def pin_gather_inverse(impl: Impl, seed=13):
+    """Cutting the gathered rows back into TP column blocks returns the shards
+    (the gather is a bijection of positions); TP = 1 is the identity."""
+    rng = np.random.default_rng(seed)
+    for TP, M, S in [(8, 4, 896), (8, 2, 2560), (1, 3, 64), (3, 5, 40)]:
+        shards = rng.integers(0, 1 << 16, size=(TP, M, S), dtype=np.uint64).astype(np.uint16)
+        got = impl.gather_shards(shards)
+        back = got.reshape(M, TP, S).transpose(1, 0, 2)
+        if not np.array_equal(back, shards):
+            return f"TP={TP} M={M} S={S}: not the inverse of the column split"
+    return None
+
+
 PINS = {
     "round_golden": pin_round_golden,
     "round_vs_torch": pin_round_vs_torch,
@@ -401,4 +439,6 @@ PINS = {
     "reduce_identities": pin_reduce_identities,
     "rmsnorm_closed_forms": pin_rmsnorm_closed_forms,
     "rmsnorm_invariants": pin_rmsnorm_invariants,
+    "gather_placement": pin_gather_placement,
+    "gather_inverse": pin_gather_inverse,
 }

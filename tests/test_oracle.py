@@ -122,6 +122,13 @@ MUTANTS = {
     "rms_width_off_by_one": ("rmsnorm", lambda: _with(rmsnorm=_rms_numpy(width=HIDDEN - 1))),
     "rms_no_gamma": ("rmsnorm", lambda: _with(rmsnorm=_rms_numpy(use_gamma=False))),
     "rms_sum_not_mean": ("rmsnorm", lambda: _with(rmsnorm=_rms_numpy(width=1))),
+    "gather_rank_major_rows": ("gather", lambda: _with(
+        gather_shards=lambda sh: np.ascontiguousarray(sh).reshape(sh.shape[1], -1))),
+    "gather_reversed_ranks": ("gather", lambda: _with(
+        gather_shards=lambda sh: oracle.gather_shards(sh[::-1].copy()))),
+    "gather_drops_a_column": ("gather", lambda: _with(
+        gather_shards=lambda sh: np.concatenate(
+            [oracle.gather_shards(sh)[:, 1:], oracle.gather_shards(sh)[:, :1] * 0], axis=1))),
 }
 
 
