@@ -20,6 +20,10 @@ What each function follows (the vLLM DSpark drafter pages):
 * ``rmsnorm`` -- "drafter/comm" module text ("FP32 sum of squares, rsqrt(sum /
   7168 + eps), x * rstd * w rounded once") and ``ArNorm.kernel``'s last block.
   Evaluated in binary64 and rounded once.
+* ``decode_gemm_logits`` -- "drafter/linears", ``draft_logits``: the lm_head GEMM
+  sliced to its first n_out (org_vocab_size) columns, optional tanh soft cap,
+  scale; binary64, one rounding (the fused-epilogue reading of the pages' BF16
+  ops).
 * ``gather_shards`` -- "drafter/comm", ``Gather`` docstring and module text:
   every rank's [M, S] shard at columns r*S.. of the [M, TP*S] row; a byte move.
 * ``rmsnorm_f32_steps`` -- diagnostic: the same formula in the binary32 steps the
@@ -66,6 +70,10 @@ def _load():
             fn = getattr(lib, name)
             fn.argtypes = [u16p, u16p, u16p, ctypes.c_int, ctypes.c_int, ctypes.c_float]
             fn.restype = None
+        lib.oracle_decode_gemm_logits.argtypes = [u16p, u16p, u16p, ctypes.c_int, ctypes.c_int,
+                                                  ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                                                  ctypes.c_double, ctypes.c_int]
+        lib.oracle_decode_gemm_logits.restype = None
         lib.oracle_gather_shards.argtypes = [u16p, ctypes.c_int, ctypes.c_int, ctypes.c_int, u16p]
         lib.oracle_gather_shards.restype = None
         lib.oracle_max_threads.argtypes = []
@@ -149,6 +157,24 @@ def decode_gemm(x, W, cols=None, threads=0):
     _load().oracle_decode_gemm(_ptr(x), _ptr(W), _ptr(out), M, N, K,
                                c.ctypes.data_as(ctypes.POINTER(ctypes.c_int)), c.size,
                                threads)
+    return out
+
+
+def decode_gemm_logits(x, W, n_out=None, soft_cap=0.0, scale=1.0, threads=0):
+    """BF16 patterns [M, n_out] of scale * cap * tanh((x @ W[:n_out]^T) / cap)
+    (no tanh when soft_cap <= 0), binary64, one rounding."""
+    x = _u16(x)
+    W = _u16(W)
+    M, K = x.shape
+    N, K2 = W.shape
+    if K2 != K:
+        raise ValueError("x and W disagree on K")
+    n_out = N if n_out is None else int(n_out)
+    if not 1 <= n_out <= N:
+        raise ValueError("n_out out of range")
+    out = np.empty((M, n_out), dtype=np.uint16)
+    _load().oracle_decode_gemm_logits(_ptr(x), _ptr(W), _ptr(out), M, N, K, n_out,
+                                      float(soft_cap), float(scale), threads)
     return out
 
 

@@ -168,6 +168,41 @@ void oracle_decode_gemm_f64(const uint16_t *x, const uint16_t *W, double *sum,
     }
 }
 
+/*
+ * The lm_head logits of "drafter/linears", draft_logits: the vocab-shard GEMM,
+ * then the slice to the first n_out (org_vocab_size) columns, then, if
+ * soft_cap > 0, tanh(logits / soft_cap) * soft_cap, then logits * scale.
+ * Reading: the three element-wise steps act on the exact binary64 dot product and
+ * the result is rounded once to BF16 (the pages apply them to BF16 tensors one
+ * PyTorch op at a time; a fused epilogue rounds once). tanh is libm's binary64
+ * tanh, a library step. out is [M, n_out] row-major; W rows n_out.. are unused.
+ */
+void oracle_decode_gemm_logits(const uint16_t *x, const uint16_t *W, uint16_t *out, int M,
+                               int N, int K, int n_out, double soft_cap, double scale,
+                               int threads)
+{
+    (void)N;
+#ifdef _OPENMP
+    if (threads > 0)
+        omp_set_num_threads(threads);
+#pragma omp parallel for schedule(dynamic, 4)
+#endif
+    for (int n = 0; n < n_out; ++n) {
+        const uint16_t *w = W + (size_t)n * (size_t)K;
+        for (int m = 0; m < M; ++m) {
+            const uint16_t *xr = x + (size_t)m * (size_t)K;
+            double acc = 0.0;
+            for (int k = 0; k < K; ++k)
+                acc += oracle_bf16_to_f64(xr[k]) * oracle_bf16_to_f64(w[k]);
+            double v = acc;
+            if (soft_cap > 0.0)
+                v = tanh(v / soft_cap) * soft_cap;
+            v = v * scale;
+            out[(size_t)m * (size_t)n_out + (size_t)n] = oracle_bf16_from_f64(v);
+        }
+    }
+}
+
 /* ---- reduce + residual ------------------------------------------------------ */
 
 /*

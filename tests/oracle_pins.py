@@ -34,12 +34,13 @@ class Impl:
     reduce_residual: Callable      # (partials_bits, residual_bits|None) -> bits
     rmsnorm: Callable              # (h_bits, gamma_bits, eps) -> bits
     gather_shards: Callable = None  # (shards_bits [TP, M, S]) -> bits [M, TP*S]
+    decode_gemm_logits: Callable = None  # (x, W, n_out, soft_cap, scale) -> bits [M, n_out]
 
 
 def oracle_impl():
     import oracle
     return Impl(oracle.bf16_from_f64_array, oracle.decode_gemm, oracle.reduce_residual,
-                oracle.rmsnorm, oracle.gather_shards)
+                oracle.rmsnorm, oracle.gather_shards, oracle.decode_gemm_logits)
 
 
 # ---- helpers -----------------------------------------------------------------
@@ -388,6 +389,81 @@ def pin_rmsnorm_invariants(impl: Impl, seed=9):
     return None
 
 
+# ---- lm_head logits epilogue ---------------------------------------------------------
+
+def _decimal_tanh(q: Fraction, ctx) -> decimal.Decimal:
+    """tanh of a rational via exp in decimal arithmetic: (e^(2q) - 1) / (e^(2q) + 1)."""
+    d = ctx.divide(decimal.Decimal(q.numerator), decimal.Decimal(q.denominator))
+    e = ctx.exp(ctx.multiply(decimal.Decimal(2), d))
+    return ctx.divide(ctx.subtract(e, decimal.Decimal(1)), ctx.add(e, decimal.Decimal(1)))
+
+
+def pin_logits_closed_forms(impl: Impl):
+    """One nonzero product per output, so the dot product is exact (a*b): the result
+    must be BF16(scale * cap * tanh(a*b / cap)) with tanh from exp in 60-digit
+    decimal arithmetic, rounded once; large a*b saturates to +-cap*scale."""
+    ctx = decimal.Context(prec=60)
+    K = 64
+    cases = [(1.5, 2.0, 30.0, 1.0), (0.75, -3.0, 30.0, 0.5), (8.0, 8.0, 30.0, 1.0),
+             (3.0, 5.0, 4.0, 2.0), (256.0, 64.0, 30.0, 1.0), (-0.125, 0.25, 1.0, 3.0)]
+    # Random products (BF16 operands) near the cap, where one rounding at the end
+    # and a rounding after every step disagree often.
+    rng = np.random.default_rng(16)
+    ab = bits_to_f64(random_bf16(rng, (40, 2), std=6.0))
+    cases += [(float(a), float(b), 30.0, 0.7) for a, b in ab]
+    for a, b, cap, scale in cases:
+        x = np.zeros((1, K), dtype=np.float32)
+        W = np.zeros((2, K), dtype=np.float32)
+        x[0, 5] = a
+        W[0, 5] = b
+        W[1, 7] = 1.0  # second column: exactly 0
+        got = impl.decode_gemm_logits(bf16_bits_of(x), bf16_bits_of(W), 2, cap, scale)
+        t = _decimal_tanh(Fraction(a) * Fraction(b) / Fraction(cap), ctx)
+        v = Fraction(ctx.multiply(ctx.multiply(t, decimal.Decimal(cap)), decimal.Decimal(scale)))
+        want = em.to_bits_bf16(em.round_ne(v, em.BF16))
+        if int(got[0, 0]) != want:
+            return f"a={a} b={b} cap={cap} scale={scale}: 0x{int(got[0, 0]):04x} vs 0x{want:04x}"
+        if int(got[0, 1]) & 0x7FFF:
+            return "tanh(0) * cap * scale is not zero"
+    return None
+
+
+def pin_logits_reduce_to_gemm(impl: Impl, seed=14):
+    """No cap, scale 1: the first n_out columns of the plain GEMM, bit for bit; no
+    cap, scale 4: exactly four times those values (a power of two)."""
+    rng = np.random.default_rng(seed)
+    M, N, K = 3, 200, 256
+    x = random_bf16(rng, (M, K))
+    W = random_bf16(rng, (N, K), std=1.0 / 16)
+    full = oracle_gemm = impl.decode_gemm(x, W)
+    got = impl.decode_gemm_logits(x, W, 150, 0.0, 1.0)
+    if got.shape != (M, 150) or not np.array_equal(got, full[:, :150]):
+        return "no-cap scale-1 logits are not the GEMM's first n_out columns"
+    four = impl.decode_gemm_logits(x, W, N, 0.0, 4.0)
+    if not np.array_equal(bits_to_f64(four), 4 * bits_to_f64(oracle_gemm)):
+        return "scale 4 is not exactly four times the GEMM"
+    return None
+
+
+def pin_logits_odd_and_sliced(impl: Impl, seed=15):
+    """tanh is odd: negating W negates every logit; the slice keeps the leading
+    columns (a smaller n_out is a prefix of a larger one)."""
+    rng = np.random.default_rng(seed)
+    M, N, K = 2, 96, 128
+    x = random_bf16(rng, (M, K))
+    W = random_bf16(rng, (N, K), std=0.5)
+    a = impl.decode_gemm_logits(x, W, N, 5.0, 0.75)
+    b = impl.decode_gemm_logits(x, W ^ np.uint16(0x8000), N, 5.0, 0.75)
+    nz = (a & 0x7FFF) != 0
+    if not np.array_equal(b[nz], a[nz] ^ np.uint16(0x8000)):
+        return "negating W does not negate the logits"
+    if not np.array_equal(impl.decode_gemm_logits(x, W, 40, 5.0, 0.75), a[:, :40]):
+        return "n_out = 40 is not the first 40 columns"
+    if np.any(np.abs(bits_to_f64(a)) > 5.0 * 0.75 * (1 + 2.0 ** -8)):
+        return "a soft-capped logit exceeds cap * scale"
+    return None
+
+
 # ---- gather ---------------------------------------------------------------------------
 
 def pin_gather_placement(impl: Impl, seed=12):
@@ -439,6 +515,9 @@ PINS = {
     "reduce_identities": pin_reduce_identities,
     "rmsnorm_closed_forms": pin_rmsnorm_closed_forms,
     "rmsnorm_invariants": pin_rmsnorm_invariants,
+    "logits_closed_forms": pin_logits_closed_forms,
+    "logits_reduce_to_gemm": pin_logits_reduce_to_gemm,
+    "logits_odd_and_sliced": pin_logits_odd_and_sliced,
     "gather_placement": pin_gather_placement,
     "gather_inverse": pin_gather_inverse,
 }

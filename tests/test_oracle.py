@@ -89,6 +89,17 @@ def _reduce_fused_residual(p, r):
     return oracle.bf16_from_f64_array((s + bits_to_f64(r).astype(np.float32)).astype(np.float64))
 
 
+def _logits_numpy(x, W, n_out, cap, scale, div=True, mul=True, round_steps=False):
+    """Deliberately broken variants of the logits epilogue (on the oracle's sums)."""
+    s, _ = oracle.decode_gemm_f64(x, W[:n_out])
+    r = (lambda v: bits_to_f64(oracle.bf16_from_f64_array(v))) if round_steps else (lambda v: v)
+    v = r(s)
+    if cap > 0:
+        v = r(np.tanh(r(v / cap if div else v)))
+        v = r(v * cap) if mul else v
+    return oracle.bf16_from_f64_array(v * scale)
+
+
 def _transposed_weight(x, W):
     N, K = W.shape
     return oracle.decode_gemm(x, np.ascontiguousarray(W.reshape(K, N).T))
@@ -122,6 +133,16 @@ MUTANTS = {
     "rms_width_off_by_one": ("rmsnorm", lambda: _with(rmsnorm=_rms_numpy(width=HIDDEN - 1))),
     "rms_no_gamma": ("rmsnorm", lambda: _with(rmsnorm=_rms_numpy(use_gamma=False))),
     "rms_sum_not_mean": ("rmsnorm", lambda: _with(rmsnorm=_rms_numpy(width=1))),
+    "logits_no_division_by_cap": ("logits", lambda: _with(
+        decode_gemm_logits=lambda x, W, n, cap, sc: _logits_numpy(x, W, n, cap, sc, div=False))),
+    "logits_no_times_cap": ("logits", lambda: _with(
+        decode_gemm_logits=lambda x, W, n, cap, sc: _logits_numpy(x, W, n, cap, sc, mul=False))),
+    "logits_scale_ignored": ("logits", lambda: _with(
+        decode_gemm_logits=lambda x, W, n, cap, sc: _logits_numpy(x, W, n, cap, 1.0))),
+    "logits_slice_from_end": ("logits", lambda: _with(
+        decode_gemm_logits=lambda x, W, n, cap, sc: _logits_numpy(x, W[W.shape[0] - n:], n, cap, sc))),
+    "logits_bf16_between_ops": ("logits", lambda: _with(
+        decode_gemm_logits=lambda x, W, n, cap, sc: _logits_numpy(x, W, n, cap, sc, round_steps=True))),
     "gather_rank_major_rows": ("gather", lambda: _with(
         gather_shards=lambda sh: np.ascontiguousarray(sh).reshape(sh.shape[1], -1))),
     "gather_reversed_ranks": ("gather", lambda: _with(
