@@ -65,9 +65,10 @@ typedef enum {
 /* Row width of every reduce + RMSNorm row: 7168 ("drafter/comm", ArNorm:
  * "All-reduce of BF16 rows [M, 7168]"; the mean divides by 7168). */
 #define SKINNY_HIDDEN 7168
-/* Largest row count of decode_gemm_bf16 ("drafter/linears" module text: the
- * stream stays near HBM speed "up to 32 rows"). */
-#define SKINNY_GEMM_MAX_M 32
+/* Largest row count of decode_gemm_bf16: the pages' engine serves "up to 32
+ * rows" ("drafter/linears" module text); this library also serves 33..64 (the
+ * row cap of the pages' reduction buffers, "cutedsl/common/twoshot", cap=64). */
+#define SKINNY_GEMM_MAX_M 64
 /* Largest row count of reduce_residual_rmsnorm (the row cap of the pages'
  * reduction buffers, "cutedsl/common/twoshot", TwoShot: cap=64). */
 #define SKINNY_REDUCE_MAX_M 64
@@ -86,7 +87,7 @@ typedef enum {
  *        aligned. Read exactly once from HBM.
  *   out  [M, N] BF16, row-major (row stride N elements), 2-byte aligned. Written
  *        once; must not overlap x or W.
- *   1 <= M <= 32;  N >= 1;  K >= 8 and K % 8 == 0 (16-byte row strides).
+ *   1 <= M <= 64;  N >= 1;  K >= 8 and K % 8 == 0 (16-byte row strides).
  *   Ragged N (N % 128 != 0) and ragged K (K % 64 != 0) are handled exactly.
  *
  *   Every out element is the FP32 sum of the K products (split over K across
@@ -97,6 +98,23 @@ typedef enum {
  */
 SKINNY_API int decode_gemm_bf16(const void *x, const void *W, void *out,
                      int M, int N, int K, void *stream);
+
+/*
+ * decode_gemm_bf16_logits -- the lm_head logits with the epilogue fused
+ *   ("drafter/linears", draft_logits: the lm_head GEMM, then the slice to
+ *    org_vocab_size, then tanh(logits / soft_cap) * soft_cap if a soft cap is
+ *    set, then logits * scale.)
+ *
+ *   x [M, K], W [N, K] as for decode_gemm_bf16; out [M, n_out] BF16 (row stride
+ *   n_out). out[m][n] = BF16(scale * c(sum_k x[m,k] W[n,k])) for n < n_out, with
+ *   c(v) = soft_cap * tanh(v / soft_cap) if soft_cap > 0, else v; the epilogue
+ *   runs on the FP32 sum and rounds once (the pages apply it one BF16 tensor op
+ *   at a time). Only the first n_out weight rows are read. 1 <= n_out <= N;
+ *   soft_cap and scale finite. Other rules and errors as decode_gemm_bf16.
+ */
+SKINNY_API int decode_gemm_bf16_logits(const void *x, const void *W, void *out, int M,
+                                       int N, int K, int n_out, float soft_cap, float scale,
+                                       void *stream);
 
 /*
  * decode_gemm_bf16_noalloc -- decode_gemm_bf16 that allocates no device memory
@@ -156,6 +174,30 @@ SKINNY_API int reduce_residual_rmsnorm(const void *partials, int TP, const void 
                             const void *gamma, void *out, void *residual_out,
                             int M, float eps, void *stream);
 
+/* Largest TP and row count of gather_shards_bf16. */
+#define SKINNY_GATHER_MAX_TP 64
+#define SKINNY_GATHER_MAX_M 65535
+
+/*
+ * gather_shards_bf16 -- every rank's shard into the gathered rows, locally
+ *   ("drafter/comm": Gather -- "Every rank's [M, S] ... shard -> the [cap, TP * S]
+ *    mailbox rows", "rank r's at columns r S .."; gather_context builds
+ *    [M, 7168] from [M, 7168 / TP], gather_logits [M, V] from [M, V / TP]. Here
+ *    the TP shards are local slots, as in the pages' one-GPU stand-in of
+ *    "cutedsl/common/twoshot".)
+ *
+ *   shards  [TP, M, S] BF16, contiguous (slot r = rank r's [M, S] shard).
+ *   out     [M, TP * S] BF16: out[m][r * S + j] = shards[r][m][j]; must not
+ *           overlap shards.
+ *   1 <= TP <= 64, 1 <= M <= 65535, S >= 8 and S % 8 == 0 (16-byte fragments,
+ *   as the pages' Gather requires), both pointers 16-byte aligned.
+ *   A byte move: the values are copied unchanged (the local slots have no
+ *   sentinel, so the pages' (+0, -0) -> (+0, +0) cleaning does not apply).
+ *   Errors: SKINNY_ERR_NULL, _SHAPE, _ALIGN, _ALIAS, _DEVICE, _LAUNCH.
+ */
+SKINNY_API int gather_shards_bf16(const void *shards, int TP, int M, int S, void *out,
+                                  void *stream);
+
 /* Human-readable text of a skinny_status code (static storage). */
 SKINNY_API const char *skinny_status_string(int status);
 
@@ -192,7 +234,7 @@ typedef struct {
     int kblocks;        /* ceil(K / 64): 64-wide K blocks per tile */
     long long blocks;   /* tiles * kblocks */
     int ctas;           /* CTAs launched: min(num_sms, blocks) */
-    int mma_n;          /* padded row count the MMA runs with: 16 or 32 */
+    int mma_n;          /* padded row count the MMA runs with: 16, 32 or 64 */
     int stages;         /* shared-memory pipeline stages per CTA */
     int smem_bytes;     /* dynamic shared memory per CTA */
     int split_tiles;    /* tiles whose K range spans more than one CTA */

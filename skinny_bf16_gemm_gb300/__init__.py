@@ -8,6 +8,7 @@ operations raises.
 
     decode_gemm_bf16(x, W, out)                      out = x @ W^T (BF16)
     reduce_residual_rmsnorm(partials, residual, gamma, out, residual_out, eps)
+    gather_shards_bf16(shards, out)                  TP shards side by side
 """
 import ctypes
 import os
@@ -15,7 +16,7 @@ import os
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIBRARY = os.path.join(PKG, "libskinny.so")
 HIDDEN = 7168
-GEMM_MAX_M = 32
+GEMM_MAX_M = 64
 REDUCE_MAX_M = 64
 REDUCE_MAX_TP = 8
 
@@ -57,6 +58,10 @@ def load_library(path: str = LIBRARY):
     lib.decode_gemm_bf16.restype = i32
     lib.reduce_residual_rmsnorm.argtypes = [vp, i32, vp, vp, vp, vp, i32, f32, vp]
     lib.reduce_residual_rmsnorm.restype = i32
+    lib.decode_gemm_bf16_logits.argtypes = [vp, vp, vp, i32, i32, i32, i32, f32, f32, vp]
+    lib.decode_gemm_bf16_logits.restype = i32
+    lib.gather_shards_bf16.argtypes = [vp, i32, i32, i32, vp, vp]
+    lib.gather_shards_bf16.restype = i32
     lib.skinny_status_string.argtypes = [i32]
     lib.skinny_status_string.restype = ctypes.c_char_p
     lib.skinny_device_error.argtypes = [i32, ctypes.POINTER(i32)]
@@ -120,6 +125,24 @@ def decode_gemm_bf16(x, W, out, stream=None):
     return out
 
 
+def decode_gemm_bf16_logits(x, W, out, soft_cap=0.0, scale=1.0, stream=None):
+    """lm_head logits out[M, n_out] = scale * cap * tanh((x @ W[:n_out]^T) / cap)
+    (no tanh if soft_cap <= 0); n_out = out.shape[1] <= W.shape[0]. Returns out."""
+    _bf16_cuda(x, "x")
+    _bf16_cuda(W, "W")
+    _bf16_cuda(out, "out")
+    if x.dim() != 2 or W.dim() != 2 or out.dim() != 2 or x.shape[1] != W.shape[1] \
+            or out.shape[0] != x.shape[0]:
+        raise ValueError("x [M,K], W [N,K] and out [M,n_out] do not fit together")
+    M, K = x.shape
+    N, n_out = W.shape[0], out.shape[1]
+    st = load_library().decode_gemm_bf16_logits(x.data_ptr(), W.data_ptr(), out.data_ptr(), M,
+                                                N, K, n_out, float(soft_cap), float(scale),
+                                                _stream_handle(stream))
+    _check(st, "decode_gemm_bf16_logits")
+    return out
+
+
 def reduce_residual_rmsnorm(partials, residual, gamma, out, residual_out, eps=1e-6,
                             stream=None):
     """(out, residual_out) of the rank-order reduce + residual + RMSNorm.
@@ -142,6 +165,22 @@ def reduce_residual_rmsnorm(partials, residual, gamma, out, residual_out, eps=1e
         _stream_handle(stream))
     _check(st, "reduce_residual_rmsnorm")
     return out, residual_out
+
+
+def gather_shards_bf16(shards, out, stream=None):
+    """out[M, TP*S] = the TP shards [TP, M, S] side by side (rank r at columns r*S..).
+
+    shards, out: contiguous CUDA bfloat16 tensors. Returns ``out``.
+    """
+    _bf16_cuda(shards, "shards")
+    if shards.dim() != 3:
+        raise ValueError(f"shards must be [TP, M, S], got {tuple(shards.shape)}")
+    TP, M, S = shards.shape
+    _bf16_cuda(out, "out", (M, TP * S))
+    st = load_library().gather_shards_bf16(shards.data_ptr(), TP, M, S, out.data_ptr(),
+                                           _stream_handle(stream))
+    _check(st, "gather_shards_bf16")
+    return out
 
 
 def device_error(device=None):

@@ -163,10 +163,11 @@ int gemm_shape_ok(int M, int N, int K) {
     return SKINNY_OK;
 }
 
-int mma_n_for(int M) { return M <= 16 ? 16 : 32; }
+int mma_n_for(int M) { return M <= 16 ? 16 : (M <= 32 ? 32 : 64); }
 
 int gemm_launch(const void *x, const void *W, void *out, int M, int N, int K, void *stream,
-                int selftest, unsigned long long limit_ns) {
+                int selftest, unsigned long long limit_ns, int logits = 0, float soft_cap = 0.0f,
+                float scale = 1.0f) {
     if (!x || !W || !out) return SKINNY_ERR_NULL;
     int st = gemm_shape_ok(M, N, K);
     if (st) return st;
@@ -188,17 +189,21 @@ int gemm_launch(const void *x, const void *W, void *out, int M, int N, int K, vo
     alignas(64) CUtensorMap w_map, x_map;
     if ((st = encode_2d(enc, &w_map, W, N, K, kBlockN))) return st;
     if ((st = encode_2d(enc, &x_map, x, M, K, mma_n))) return st;
-    const GemmGeometry g = make_geometry(M, N, K, d->sms);
+    const GemmGeometry g = make_geometry(M, N, K, choose_ctas(N, d->sms));
     GemmArgs a;
     a.M = M;
     a.N = N;
     a.K = K;
     a.out = static_cast<uint16_t *>(out);
     a.partials = d->partials;
+    a.slot_floats = kSlotFloats;
     a.counters = d->counters;
     a.err = d->err;
     a.wait_limit_ns = limit_ns;
     a.selftest = selftest;
+    a.logits = logits;
+    a.soft_cap = soft_cap;
+    a.scale = scale;
     bool pdl;
     {
         std::lock_guard<std::mutex> lock(g_mutex);
@@ -217,8 +222,9 @@ int gemm_launch(const void *x, const void *W, void *out, int M, int N, int K, vo
 int gemm_launch_static(const void *x, const void *W, void *out, int M, int N, int K,
                        void *stream) {
     if (!x || !W || !out) return SKINNY_ERR_NULL;
-    int st = gemm_shape_ok(M, N, K);  // M <= 32 is also the static slots' row limit
+    int st = gemm_shape_ok(M, N, K);
     if (st) return st;
+    if (M > kStaticSlotRows) return SKINNY_ERR_SHAPE;  // the static partial tiles hold 32 rows
     if (!aligned(x, 16) || !aligned(W, 16) || !aligned(out, 2)) return SKINNY_ERR_ALIGN;
     const size_t xb = static_cast<size_t>(M) * K * 2, wb = static_cast<size_t>(N) * K * 2,
                  ob = static_cast<size_t>(M) * N * 2;
@@ -242,7 +248,8 @@ int gemm_launch_static(const void *x, const void *W, void *out, int M, int N, in
     if ((st = encode_2d(enc, &w_map, W, N, K, kBlockN))) return st;
     if ((st = encode_2d(enc, &x_map, x, M, K, mma_n))) return st;
     // At most as many CTAs as the array has partial-tile slots for.
-    const GemmGeometry g = make_geometry(M, N, K, d->sms < sc.max_ctas ? d->sms : sc.max_ctas);
+    const int ctas = choose_ctas(N, d->sms);
+    const GemmGeometry g = make_geometry(M, N, K, ctas < sc.max_ctas ? ctas : sc.max_ctas);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // The array keeps the previous call's contents: the tile counters and the
     // error word must start this call at zero.
@@ -256,10 +263,14 @@ int gemm_launch_static(const void *x, const void *W, void *out, int M, int N, in
     a.K = K;
     a.out = static_cast<uint16_t *>(out);
     a.partials = sc.partials;
+    a.slot_floats = kStaticSlotRows * kBlockN;
     a.counters = sc.counters;
     a.err = sc.err;
     a.wait_limit_ns = kWaitLimitNs;
     a.selftest = 0;
+    a.logits = 0;
+    a.soft_cap = 0.0f;
+    a.scale = 1.0f;
     bool pdl;
     {
         std::lock_guard<std::mutex> lock(g_mutex);
@@ -291,6 +302,15 @@ int decode_gemm_bf16(const void *x, const void *W, void *out, int M, int N, int 
 int decode_gemm_bf16_noalloc(const void *x, const void *W, void *out, int M, int N, int K,
                              void *stream) {
     return gemm_launch_static(x, W, out, M, N, K, stream);
+}
+
+int decode_gemm_bf16_logits(const void *x, const void *W, void *out, int M, int N, int K,
+                            int n_out, float soft_cap, float scale, void *stream) {
+    if (n_out < 1 || n_out > N) return SKINNY_ERR_SHAPE;
+    if (!std::isfinite(soft_cap) || !std::isfinite(scale)) return SKINNY_ERR_ARG;
+    // Only the first n_out weight rows are read: the same GEMM with N = n_out.
+    return gemm_launch(x, W, out, M, n_out, K, stream, 0, kWaitLimitNs, 1,
+                       soft_cap > 0.0f ? soft_cap : 0.0f, scale);
 }
 
 int skinny_watchdog_selftest(const void *x, const void *W, void *out, int M, int N, int K,
@@ -336,6 +356,31 @@ int reduce_residual_rmsnorm(const void *partials, int TP, const void *residual,
                                           reduce_ctas_per_row(M),
                                           static_cast<cudaStream_t>(stream), pdl);
     if (e != cudaSuccess) {
+        cudaGetLastError();
+        return SKINNY_ERR_LAUNCH;
+    }
+    return SKINNY_OK;
+}
+
+int gather_shards_bf16(const void *shards, int TP, int M, int S, void *out, void *stream) {
+    if (!shards || !out) return SKINNY_ERR_NULL;
+    if (TP < 1 || TP > SKINNY_GATHER_MAX_TP || M < 1 || M > SKINNY_GATHER_MAX_M || S < 8 ||
+        (S % 8) != 0 || static_cast<long long>(TP) * S > (1LL << 30))
+        return SKINNY_ERR_SHAPE;
+    if (!aligned(shards, 16) || !aligned(out, 16)) return SKINNY_ERR_ALIGN;
+    const size_t bytes = static_cast<size_t>(TP) * M * S * 2;
+    if (overlaps(out, bytes, shards, bytes)) return SKINNY_ERR_ALIAS;
+    int dev, st;
+    if ((st = current_device(&dev))) return st;
+    DeviceState *d = nullptr;
+    if ((st = device_state(dev, &d))) return st;
+    if ((st = check_device_pointer(shards, dev)) || (st = check_device_pointer(out, dev))) return st;
+    bool pdl;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        pdl = g_pdl;
+    }
+    if (launch_gather(shards, TP, M, S, out, static_cast<cudaStream_t>(stream), pdl) != cudaSuccess) {
         cudaGetLastError();
         return SKINNY_ERR_LAUNCH;
     }
@@ -409,7 +454,7 @@ int skinny_gemm_plan_query(int M, int N, int K, int num_sms, skinny_gemm_plan *p
     if (num_sms < 1) return SKINNY_ERR_ARG;
     int st = gemm_shape_ok(M, N, K);
     if (st) return st;
-    const GemmGeometry g = make_geometry(M, N, K, num_sms);
+    const GemmGeometry g = make_geometry(M, N, K, choose_ctas(N, num_sms));
     plan->tiles = g.tiles;
     plan->kblocks = g.kblocks;
     plan->blocks = g.blocks;
@@ -435,7 +480,7 @@ int skinny_gemm_plan_query(int M, int N, int K, int num_sms, skinny_gemm_plan *p
 int skinny_gemm_cta_pieces(int M, int N, int K, int num_sms, int cta, int *tile, int *kb0,
                            int *kb1, int *slot, int max_pieces) {
     if (!tile || !kb0 || !kb1 || !slot || num_sms < 1 || gemm_shape_ok(M, N, K)) return -1;
-    const GemmGeometry g = make_geometry(M, N, K, num_sms);
+    const GemmGeometry g = make_geometry(M, N, K, choose_ctas(N, num_sms));
     if (cta < 0 || cta >= g.ctas) return -1;
     const int n = cta_piece_count(g, cta);
     for (int q = 0; q < n && q < max_pieces; ++q) {

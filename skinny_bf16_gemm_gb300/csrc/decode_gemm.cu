@@ -37,9 +37,9 @@ namespace {
 
 constexpr int kThreads = 192;
 constexpr int kEpilogueThreads = 128;
-constexpr int kTmemCols = 64;          // two accumulator buffers of 32 columns
 constexpr int kWBytes = kBlockN * kBlockK * 2;
 constexpr uint64_t kDrainLimitNs = 200000000ull;  // 0.2 s for copies already issued
+constexpr int kL2PrefetchBlocks = 6;  // weight blocks prefetched to L2 before the ring's
 
 // MP: padded row count (MMA N). STAGES: shared-memory ring depth. The deep ring
 // (~185 KB) keeps the most bytes in flight; the shallow one (~92-101 KB) lets the
@@ -48,6 +48,8 @@ constexpr uint64_t kDrainLimitNs = 200000000ull;  // 0.2 s for copies already is
 template <int MP, int STAGES>
 struct Layout {
     static constexpr int kStages = STAGES;
+    static constexpr int kAccCols = MP == 64 ? 64 : 32;  // TMEM columns per accumulator
+    static constexpr int kTmemCols = 2 * kAccCols;       // two accumulator buffers
     static constexpr int kXBytes = MP * kBlockK * 2;
     static constexpr int kStageBytes = kWBytes + kXBytes;
     static constexpr int kBarOffset = kStages * kStageBytes;
@@ -100,6 +102,14 @@ __device__ __forceinline__ uint16_t to_bf16_bits(float v) {
     return __bfloat16_as_ushort(__float2bfloat16_rn(v));
 }
 
+// The value an output element is rounded from: the FP32 sum itself, or for the
+// lm_head logits ("drafter/linears", draft_logits) the soft-capped, scaled sum.
+__device__ __forceinline__ float output_value(float v, const GemmArgs &a) {
+    if (!a.logits) return v;
+    if (a.soft_cap > 0.0f) v = __fmul_rn(tanhf(__fdiv_rn(v, a.soft_cap)), a.soft_cap);
+    return __fmul_rn(v, a.scale);
+}
+
 template <int MP, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_gemm_kernel(const __grid_constant__ CUtensorMap w_map,
@@ -143,7 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::fence_barrier_init();
     }
     if (warp == 0) {
-        ptx::tmem_alloc(sbase + L::kMiscOffset, kTmemCols);
+        ptx::tmem_alloc(sbase + L::kMiscOffset, L::kTmemCols);
         ptx::tmem_relinquish();
     }
     ptx::tc_fence_before_sync();
@@ -152,8 +162,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem_base = misc[0];
     volatile uint32_t *abort_flag = misc + 1;
 
-    // Dependent kernels may be scheduled now; they wait for this grid before
-    // touching anything it writes.
+    // The next kernel in the stream may launch now: its CTAs fit beside this one
+    // (shallow ring), set up and stream their first weights while this grid
+    // runs, and wait for it before touching anything it writes.
     ptx::pdl_launch_dependents();
 
     const int pieces = cta_piece_count(g, cta);
@@ -182,6 +193,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::mbar_arrive_expect_tx(bar_full + 8 * j, L::kStageBytes);
                 armed |= 1u << j;
                 ptx::tma_load_2d(st, &w_map, bar_full + 8 * j, kb * kBlockK, t * kBlockN, pol_w);
+            }
+            // The blocks after the ring's worth go to L2 ahead of time.
+            const long long npf = total - npre < kL2PrefetchBlocks ? total - npre : kL2PrefetchBlocks;
+            for (long long j = npre; j < npre + npf; ++j) {
+                const long long blk = b0 + j;
+                ptx::tma_prefetch_l2_2d(&w_map, static_cast<int>(blk % g.kblocks) * kBlockK,
+                                        static_cast<int>(blk / g.kblocks) * kBlockN);
             }
             ptx::pdl_wait();  // x may be the predecessor's output
             for (int j = 0; j < npre; ++j) {
@@ -238,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 ptx::tc_fence_after_sync();
-                const uint32_t d_tmem = tmem_base + b * 32;
+                const uint32_t d_tmem = tmem_base + b * L::kAccCols;
                 for (int kb = p.kb0; kb < p.kb1; ++kb) {
                     r = bounded_wait(bar_full + 8 * s, ph, abort_flag, limit);
                     if (r != kWaitDone) {
@@ -274,54 +292,150 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quarter = warp & 3;              // TMEM lanes 32*quarter .. +31
         const int row = quarter * 32 + lane;       // weight row within the tile
         const int etid = threadIdx.x - 64;
-        // Tiles this CTA arrived last at: tile, first and last contributor, packed
-        // (register-resident; at most two).
+        const int slot_bytes = g.M * kBlockN * static_cast<int>(sizeof(float));
+        const int ring_slots = L::kRingBytes / slot_bytes;
+        const float *staging = reinterpret_cast<const float *>(smem);
+        uint32_t fix_phase = 0;
+        bool fix_pending = false;
+
+        // Finish shared tile t: add the FP32 partial sums of CTAs first..last in K
+        // (= CTA) order and round once. Partials are pulled into the ring (free
+        // by then) with bulk copies, all in flight at once. own != nullptr: this
+        // CTA's partial is in registers and is not copied. false = aborted.
+        auto finish_tile = [&](int t, int first, int last, const float *own) -> bool {
+            float sum[MP];
+#pragma unroll
+            for (int m = 0; m < MP; ++m) sum[m] = 0.0f;
+            bool started = false;
+            int c0 = first;
+            while (c0 <= last) {
+                // The next chunk of contributors whose copies fit in the ring.
+                int c1 = c0, copies = 0;
+                while (c1 <= last && (copies < ring_slots || (own && c1 == cta))) {
+                    if (!(own && c1 == cta)) ++copies;
+                    ++c1;
+                }
+                if (copies > 0) {
+                    if (etid == 0) {
+                        __threadfence();
+                        ptx::fence_proxy_async_global();
+                        ptx::mbar_arrive_expect_tx(bar_fix, static_cast<uint32_t>(copies * slot_bytes));
+                        int i = 0;
+                        for (int c = c0; c < c1; ++c) {
+                            if (own && c == cta) continue;
+                            ptx::bulk_load(sbase + i * slot_bytes,
+                                           args.partials + static_cast<size_t>(partial_slot(g, c, t)) * args.slot_floats,
+                                           slot_bytes, bar_fix);
+                            ++i;
+                        }
+                    }
+                    fix_pending = true;
+                    const int r = bounded_wait(bar_fix, fix_phase, abort_flag, limit);
+                    if (r == kWaitTimeout) raise_error(args.err, abort_flag, kErrEpilogueWait);
+                    if (epilogue_any(r != kWaitDone)) return false;
+                    fix_pending = false;
+                    fix_phase ^= 1u;
+                }
+                int i = 0;
+                for (int c = c0; c < c1; ++c) {
+                    const bool mine = own && c == cta;
+                    const float *src = staging + static_cast<size_t>(i) * g.M * kBlockN + row;
+#pragma unroll
+                    for (int m = 0; m < MP; ++m) {
+                        if (m < g.M) {
+                            const float v = mine ? own[m] : src[m * kBlockN];
+                            sum[m] = started ? __fadd_rn(sum[m], v) : v;
+                        }
+                    }
+                    started = true;
+                    if (!mine) ++i;
+                }
+                ptx::named_barrier_sync(1, kEpilogueThreads);  // the ring is refilled next
+                c0 = c1;
+            }
+            const int n = t * kBlockN + row;
+            if (n < g.N) {
+#pragma unroll
+                for (int m = 0; m < MP; ++m)
+                    if (m < g.M)
+                        args.out[static_cast<size_t>(m) * g.N + n] = to_bf16_bits(output_value(sum[m], args));
+            }
+            return true;
+        };
+
+        // Shared tiles this CTA arrived last at while streaming: tile, first and
+        // last contributor (register-resident; at most two -- only a range's first
+        // and last pieces can be partial). They are finished once the ring is free.
         int4 fin[2] = {make_int4(0, 0, 0, 0), make_int4(0, 0, 0, 0)};
         int fin_count = 0;
-        bool fix_pending = false;
+        bool aborted = false;
         for (int q = 0; q < pieces; ++q) {
             const Piece p = cta_piece(g, cta, q);
             const int b = q & 1;
             const uint32_t aph = (q >> 1) & 1;
             const int r = bounded_wait(bar_acc_full + 8 * b, aph, abort_flag, limit);
             if (r == kWaitTimeout) raise_error(args.err, abort_flag, kErrEpilogueWait);
-            if (epilogue_any(r != kWaitDone)) break;
+            if (epilogue_any(r != kWaitDone)) {
+                aborted = true;
+                break;
+            }
             ptx::tc_fence_after_sync();
             float acc[MP];
             {
-                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + b * 32;
-                uint32_t v[16];
-                ptx::tmem_ld16(taddr, v);
-                ptx::tmem_ld_wait(v);
+                const uint32_t taddr =
+                    tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + b * L::kAccCols;
 #pragma unroll
-                for (int i = 0; i < 16; ++i) acc[i] = __uint_as_float(v[i]);
-                if constexpr (MP == 32) {
-                    ptx::tmem_ld16(taddr + 16, v);
+                for (int c = 0; c < MP; c += 16) {
+                    uint32_t v[16];
+                    ptx::tmem_ld16(taddr + c, v);
                     ptx::tmem_ld_wait(v);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) acc[16 + i] = __uint_as_float(v[i]);
+                    for (int i = 0; i < 16; ++i) acc[c + i] = __uint_as_float(v[i]);
                 }
             }
             ptx::tc_fence_before_sync();
             ptx::mbar_arrive(bar_acc_empty + 8 * b);  // the MMA may reuse this buffer
 
             const int n = p.tile * kBlockN + row;
-            const bool in_range = n < g.N;
             if (p.kb0 == 0 && p.kb1 == g.kblocks) {
                 // Whole tile in this CTA: round once and store.
-                if (in_range) {
+                if (n < g.N) {
 #pragma unroll
                     for (int m = 0; m < MP; ++m)
-                        if (m < g.M) args.out[static_cast<size_t>(m) * g.N + n] = to_bf16_bits(acc[m]);
+                        if (m < g.M)
+                            args.out[static_cast<size_t>(m) * g.N + n] =
+                                to_bf16_bits(output_value(acc[m], args));
                 }
                 continue;
             }
-            // Shared tile: publish this CTA's partial and count the arrival. The
-            // CTA that arrives last finishes the tile, but only after its own
-            // pieces are done (the shared-memory ring is free then).
             int first, last;
             tile_contributors(g, p.tile, first, last);
-            float *mine = args.partials + static_cast<size_t>(partial_slot(g, cta, p.tile)) * kSlotFloats;
+            if (q == pieces - 1) {
+                // This CTA's last piece: the ring is free. If every other
+                // contributor has arrived already -- the usual case, they covered
+                // this tile at the start of their ranges -- finish the tile now
+                // from their partials and this CTA's registers.
+                if (etid == 0) {
+                    const unsigned others = static_cast<unsigned>(last - first);
+                    const bool all_in = ptx::ld_acquire_gpu(args.counters + first) == others;
+                    if (all_in) args.counters[first] = 0u;  // re-armed for the next call
+                    misc[2] = all_in ? 1u : 0u;
+                }
+                ptx::named_barrier_sync(1, kEpilogueThreads);
+                const bool direct = misc[2] != 0u;
+                ptx::named_barrier_sync(1, kEpilogueThreads);  // misc[2] is reused below
+                if (direct) {
+                    if (!finish_tile(p.tile, first, last, acc)) {
+                        aborted = true;
+                        break;
+                    }
+                    continue;
+                }
+            }
+            // Publish this CTA's partial and count the arrival; the CTA that
+            // arrives last finishes the tile once its own pieces are done.
+            float *mine =
+                args.partials + static_cast<size_t>(partial_slot(g, cta, p.tile)) * args.slot_floats;
 #pragma unroll
             for (int m = 0; m < MP; ++m)
                 if (m < g.M) __stcg(mine + m * kBlockN + row, acc[m]);
@@ -336,7 +450,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ptx::named_barrier_sync(1, kEpilogueThreads);
             if (misc[2] != 0u) {
-                // Only a range's first and last pieces can be partial.
                 const int4 rec = make_int4(p.tile, first, last, 0);
                 if (fin_count == 0) fin[0] = rec;
                 else fin[1] = rec;
@@ -344,71 +457,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ptx::named_barrier_sync(1, kEpilogueThreads);  // misc[2] is reused next piece
         }
-
-        // Finish the shared tiles this CTA arrived last at (at most two: only a
-        // range's first and last pieces can be partial). Every partial, this
-        // CTA's own included, is pulled into the free ring with bulk copies --
-        // all in flight at once -- and added in K (= CTA) order.
-        if (!epilogue_any(*abort_flag != 0u)) {
-            const int slot_bytes = g.M * kBlockN * static_cast<int>(sizeof(float));
-            const int cap = L::kRingBytes / slot_bytes;
-            const float *staging = reinterpret_cast<const float *>(smem);
-            uint32_t fix_phase = 0;
-            bool failed = false;
-            for (int f = 0; f < fin_count && !failed; ++f) {
-                const int4 rec = f == 0 ? fin[0] : fin[1];
-                const int t = rec.x, first = rec.y, last = rec.z;
-                float sum[MP];
-#pragma unroll
-                for (int m = 0; m < MP; ++m) sum[m] = 0.0f;
-                for (int c0 = first; c0 <= last; c0 += cap) {
-                    const int c1 = last + 1 < c0 + cap ? last + 1 : c0 + cap;
-                    if (etid == 0) {
-                        __threadfence();
-                        ptx::fence_proxy_async_global();
-                        ptx::mbar_arrive_expect_tx(bar_fix, static_cast<uint32_t>((c1 - c0) * slot_bytes));
-                        for (int c = c0; c < c1; ++c)
-                            ptx::bulk_load(sbase + (c - c0) * slot_bytes,
-                                           args.partials + static_cast<size_t>(partial_slot(g, c, t)) * kSlotFloats,
-                                           slot_bytes, bar_fix);
-                    }
-                    fix_pending = true;
-                    const int r = bounded_wait(bar_fix, fix_phase, abort_flag, limit);
-                    if (r == kWaitTimeout) raise_error(args.err, abort_flag, kErrEpilogueWait);
-                    if (epilogue_any(r != kWaitDone)) {
-                        failed = true;
-                        break;
-                    }
-                    fix_pending = false;
-                    fix_phase ^= 1u;
-                    for (int c = c0; c < c1; ++c) {
-                        const float *src = staging + static_cast<size_t>(c - c0) * g.M * kBlockN + row;
-#pragma unroll
-                        for (int m = 0; m < MP; ++m) {
-                            if (m < g.M) {
-                                const float v = src[m * kBlockN];
-                                sum[m] = c == first ? v : __fadd_rn(sum[m], v);
-                            }
-                        }
-                    }
-                    ptx::named_barrier_sync(1, kEpilogueThreads);  // staging is refilled next
-                }
-                if (failed) break;
-                const int n = t * kBlockN + row;
-                if (n < g.N) {
-#pragma unroll
-                    for (int m = 0; m < MP; ++m)
-                        if (m < g.M) args.out[static_cast<size_t>(m) * g.N + n] = to_bf16_bits(sum[m]);
-                }
-            }
-            if (fix_pending) {
-                // Copies still in flight must land before the CTA's memory is released.
-                const uint64_t t0 = ptx::global_timer_ns();
-                while (!ptx::mbar_try_wait(bar_fix, fix_phase)) {
-                    if (ptx::global_timer_ns() - t0 > kDrainLimitNs) {
-                        atomicOr(args.err, kErrDrain);
-                        break;
-                    }
+        for (int f = 0; f < fin_count && !aborted; ++f) {
+            const int4 rec = f == 0 ? fin[0] : fin[1];
+            if (!finish_tile(rec.x, rec.y, rec.z, nullptr)) aborted = true;
+        }
+        if (fix_pending) {
+            // Copies still in flight must land before the CTA's memory is released.
+            const uint64_t t0 = ptx::global_timer_ns();
+            while (!ptx::mbar_try_wait(bar_fix, fix_phase)) {
+                if (ptx::global_timer_ns() - t0 > kDrainLimitNs) {
+                    atomicOr(args.err, kErrDrain);
+                    break;
                 }
             }
         }
@@ -445,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (warp == 0) {
         ptx::tc_fence_after_sync();
-        ptx::tmem_dealloc(tmem_base, kTmemCols);
+        ptx::tmem_dealloc(tmem_base, L::kTmemCols);
     }
 }
 
@@ -476,13 +535,15 @@ cudaError_t launch_variant(const CUtensorMap &w_map, const CUtensorMap &x_map,
     return cudaLaunchKernelEx(&cfg, decode_gemm_kernel<MP, STAGES>, w_map, x_map, args);
 }
 
-constexpr int kDeepStages16 = 10, kDeepStages32 = 9, kShallowStages = 5;
+constexpr int kDeepStages16 = 10, kDeepStages32 = 9, kDeepStages64 = 7;
+constexpr int kShallowStages = 5, kShallowStages64 = 4;
 
 }  // namespace
 
 // The shallow ring goes with programmatic dependent launch (consecutive kernels
 // overlap on each SM); the deep ring otherwise.
 int gemm_stages(int mma_n, bool pdl) {
+    if (mma_n == 64) return pdl ? kShallowStages64 : kDeepStages64;
     if (pdl) return kShallowStages;
     return mma_n == 16 ? kDeepStages16 : kDeepStages32;
 }
@@ -490,7 +551,9 @@ int gemm_stages(int mma_n, bool pdl) {
 int gemm_smem_bytes(int mma_n, bool pdl) {
     if (mma_n == 16)
         return pdl ? Layout<16, kShallowStages>::kDynamicBytes : Layout<16, kDeepStages16>::kDynamicBytes;
-    return pdl ? Layout<32, kShallowStages>::kDynamicBytes : Layout<32, kDeepStages32>::kDynamicBytes;
+    if (mma_n == 32)
+        return pdl ? Layout<32, kShallowStages>::kDynamicBytes : Layout<32, kDeepStages32>::kDynamicBytes;
+    return pdl ? Layout<64, kShallowStages64>::kDynamicBytes : Layout<64, kDeepStages64>::kDynamicBytes;
 }
 
 cudaError_t launch_decode_gemm(const CUtensorMap &w_map, const CUtensorMap &x_map,
@@ -500,8 +563,12 @@ cudaError_t launch_decode_gemm(const CUtensorMap &w_map, const CUtensorMap &x_ma
         if (pdl) return launch_variant<16, kShallowStages>(w_map, x_map, args, ctas, stream, pdl, device);
         return launch_variant<16, kDeepStages16>(w_map, x_map, args, ctas, stream, pdl, device);
     }
-    if (pdl) return launch_variant<32, kShallowStages>(w_map, x_map, args, ctas, stream, pdl, device);
-    return launch_variant<32, kDeepStages32>(w_map, x_map, args, ctas, stream, pdl, device);
+    if (mma_n == 32) {
+        if (pdl) return launch_variant<32, kShallowStages>(w_map, x_map, args, ctas, stream, pdl, device);
+        return launch_variant<32, kDeepStages32>(w_map, x_map, args, ctas, stream, pdl, device);
+    }
+    if (pdl) return launch_variant<64, kShallowStages64>(w_map, x_map, args, ctas, stream, pdl, device);
+    return launch_variant<64, kDeepStages64>(w_map, x_map, args, ctas, stream, pdl, device);
 }
 
 }  // namespace skinny
@@ -517,7 +584,7 @@ namespace skinny {
 namespace {
 
 constexpr size_t kStaticPartialBytes =
-    static_cast<size_t>(2) * kStaticScratchCtas * kSlotFloats * sizeof(float);
+    static_cast<size_t>(2) * kStaticScratchCtas * kStaticSlotRows * kBlockN * sizeof(float);
 constexpr size_t kStaticCounterBytes = 1024;  // >= kStaticScratchCtas counters, 256-aligned
 constexpr size_t kStaticScratchBytes = kStaticPartialBytes + kStaticCounterBytes + 256;
 static_assert(kStaticScratchCtas * sizeof(unsigned) <= kStaticCounterBytes, "counter space");

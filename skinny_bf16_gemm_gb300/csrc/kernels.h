@@ -20,11 +20,16 @@ enum ErrorBits : int {
 struct GemmArgs {
     int M, N, K;
     uint16_t *out;          // [M, N] BF16 patterns
-    float *partials;        // [2 * ctas][32][128] FP32 split-K partial tiles
+    float *partials;        // [2 * ctas][slot rows][128] FP32 split-K partial tiles
+    int slot_floats;        // floats from one partial tile to the next
     unsigned *counters;     // [ctas] arrival counters, zero between calls
     int *err;               // device error word
     unsigned long long wait_limit_ns;
     int selftest;           // 1: the MMA role waits on a barrier nothing completes
+    // lm_head epilogue (logits = 1): v = soft_cap > 0 ? soft_cap * tanh(v / soft_cap)
+    // : v; v *= scale; applied to the FP32 sum before the one BF16 rounding.
+    int logits;
+    float soft_cap, scale;
 };
 
 // Pipeline depth and shared memory of the decode GEMM for a padded row count,
@@ -39,9 +44,10 @@ cudaError_t launch_decode_gemm(const CUtensorMap &w_map, const CUtensorMap &x_ma
 
 // Split-K scratch held in a static device array (decode_gemm_bf16_noalloc).
 constexpr int kStaticScratchCtas = 160;   // CTAs the array holds partial tiles for
+constexpr int kStaticSlotRows = 32;       // rows of x a static partial tile holds
 
 struct StaticScratch {
-    float *partials;      // [2 * max_ctas][32][128] FP32
+    float *partials;      // [2 * max_ctas][kStaticSlotRows][128] FP32
     unsigned *counters;   // [max_ctas], contiguous with err
     int *err;             // error word, right after the counter space
     size_t zero_bytes;    // bytes from `counters` through `err` that must start at zero
@@ -57,5 +63,9 @@ cudaError_t static_scratch_for_current_device(StaticScratch *out);
 cudaError_t launch_reduce_rmsnorm(const void *partials, int TP, const void *residual,
                                   const void *gamma, void *out, void *residual_out, int M,
                                   float eps, int ctas_per_row, cudaStream_t stream, bool pdl);
+
+// Gather TP shards [TP, M, S] into rows [M, TP * S] (S a multiple of 8).
+cudaError_t launch_gather(const void *shards, int TP, int M, int S, void *out,
+                          cudaStream_t stream, bool pdl);
 
 }  // namespace skinny

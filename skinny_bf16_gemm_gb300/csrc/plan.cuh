@@ -15,8 +15,8 @@ namespace skinny {
 
 constexpr int kBlockN = 128;       // weight rows per tile = MMA M
 constexpr int kBlockK = 64;        // K per pipeline stage: 128 bytes of BF16
-constexpr int kMaxM = 32;          // rows of x (MMA N is 16 or 32)
-constexpr int kSlotFloats = kMaxM * kBlockN;  // one FP32 partial tile [m][row]
+constexpr int kMaxM = 64;          // rows of x (MMA N is 16, 32 or 64)
+constexpr int kSlotFloats = kMaxM * kBlockN;  // one FP32 partial tile [m][row] (device scratch)
 
 struct GemmGeometry {
     int M, N, K;
@@ -36,6 +36,16 @@ __host__ __device__ inline GemmGeometry make_geometry(int M, int N, int K, int n
     g.blocks = static_cast<long long>(g.tiles) * g.kblocks;
     g.ctas = static_cast<int>(g.blocks < num_sms ? g.blocks : num_sms);
     return g;
+}
+
+// CTAs to launch on a device with num_sms SMs. When the tiles alone nearly fill
+// the GPU (at least 90 % of the SMs), each CTA takes one whole tile: no tile is
+// shared, so there is no split-K fix-up, and the few idle SMs cost less than the
+// fix-ups would. Otherwise one CTA per SM with the stream-K split.
+__host__ __device__ inline int choose_ctas(int N, int num_sms) {
+    const int tiles = (N + kBlockN - 1) / kBlockN;
+    if (tiles <= num_sms && tiles * 10 >= num_sms * 9) return tiles;
+    return num_sms;
 }
 
 // First weight block of CTA c (c = ctas gives the end of the last range).

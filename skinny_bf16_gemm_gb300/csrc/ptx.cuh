@@ -82,6 +82,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// Prefetch a 2-D tile of a tensor into L2 (no shared memory, no completion).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *map, int32_t c0, int32_t c1) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1)
+                 : "memory");
+}
+
 // Non-tensor bulk copy global -> this CTA's shared memory (16-byte aligned
 // addresses, size a multiple of 16), completion counted in bytes on `bar`.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
@@ -190,6 +198,14 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {
            | (1u << 10)                               // B format: BF16
            | (static_cast<uint32_t>(n >> 3) << 17)    // N / 8
            | (static_cast<uint32_t>(m >> 4) << 24);   // M / 16
+}
+
+// ---- global memory ---------------------------------------------------------------
+
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
 }
 
 // ---- clusters --------------------------------------------------------------------

@@ -65,7 +65,9 @@ def test_header_constants_match_the_pages():
     text = open(HEADER).read()
     consts = dict(re.findall(r"#define (SKINNY_\w+) (\d+)", text))
     assert int(consts["SKINNY_HIDDEN"]) == facts["hidden"] == sk.HIDDEN
-    assert int(consts["SKINNY_GEMM_MAX_M"]) == facts["warp_rows"] == sk.GEMM_MAX_M
+    # The pages' engine serves up to 32 rows; the library serves up to the row cap.
+    assert facts["warp_rows"] <= int(consts["SKINNY_GEMM_MAX_M"]) == facts["twoshot_cap"]
+    assert int(consts["SKINNY_GEMM_MAX_M"]) == sk.GEMM_MAX_M
     assert int(consts["SKINNY_REDUCE_MAX_M"]) == facts["twoshot_cap"] == sk.REDUCE_MAX_M
     # The ArNorm geometry the pages print: 8 CTAs x 112 fragments x 8 BF16 = 7168.
     assert facts["ar_ctas"] * facts["ar_frags_per_cta"] * facts["fragment_bf16"] == facts["hidden"]
@@ -89,12 +91,12 @@ def test_accepted_shapes_cover_the_pages_gate(lib):
     assert not _gate(7168, 18432, facts)
     for n in (16, 2048, 4096, 7168, 12288, 18432, 20480):
         for k in (128, 7168, 14336, 18432):
-            for m in (1, 32):
+            for m in (1, 32, 64):
                 sk.gemm_plan(m, n, k, 152)
 
 
 @pytest.mark.parametrize("args,code", [
-    ((0, 16, 64), 2), ((33, 16, 64), 2), ((4, 0, 64), 2), ((4, 16, 0), 2), ((4, 16, 12), 2),
+    ((0, 16, 64), 2), ((65, 16, 64), 2), ((4, 0, 64), 2), ((4, 16, 0), 2), ((4, 16, 12), 2),
 ])
 def test_gemm_rejects_shapes_before_cuda(lib, args, code):
     M, N, K = args
@@ -139,6 +141,21 @@ def test_reduce_rejects_before_cuda(lib):
     assert f(part, 8, res, gam, out, res + 16, 2, 1e-6, None) == 6     # partial residual overlap
 
 
+def test_gather_rejects_before_cuda(lib):
+    buf = ctypes.create_string_buffer(1 << 20)
+    p = ctypes.addressof(buf) + (-ctypes.addressof(buf)) % 256
+    f = lib.gather_shards_bf16
+    assert f(None, 8, 4, 64, p + 65536, None) == 1
+    assert f(p, 8, 4, 64, None, None) == 1
+    assert f(p, 0, 4, 64, p + 65536, None) == 2
+    assert f(p, 65, 4, 64, p + 65536, None) == 2
+    assert f(p, 8, 0, 64, p + 65536, None) == 2
+    assert f(p, 8, 4, 12, p + 65536, None) == 2
+    assert f(p, 8, 4, 0, p + 65536, None) == 2
+    assert f(p + 8, 8, 4, 64, p + 65536, None) == 3
+    assert f(p, 8, 4, 64, p + 2048, None) == 6
+
+
 def test_calls_without_a_device_report_device_error(lib):
     """With valid arguments but no CUDA device the call fails cleanly."""
     import torch
@@ -149,10 +166,11 @@ def test_calls_without_a_device_report_device_error(lib):
     assert lib.decode_gemm_bf16(p, p + 4096, p + 65536, 4, 16, 64, None) == 4
 
 
-SHAPES = [(1, 16, 64, 152), (4, 2048, 7168, 152), (16, 18432, 7168, 152),
+SHAPES = [(1, 16, 64, 152), (4, 2048, 7168, 152), (16, 18432, 7168, 152), (16, 18432, 7168, 148),
           (16, 7168, 18432, 152), (32, 20480, 7168, 152), (3, 200, 136, 152),
           (8, 128, 64, 152), (5, 12288, 7168, 148), (2, 4096, 7168, 7), (1, 1, 8, 152),
-          (32, 1000, 1000, 152), (7, 300, 4096, 64)]
+          (32, 1000, 1000, 152), (7, 300, 4096, 64), (64, 18432, 7168, 152),
+          (48, 7168, 14336, 152), (33, 130, 72, 152)]
 
 
 @pytest.mark.parametrize("M,N,K,sms", SHAPES)
@@ -160,8 +178,14 @@ def test_work_split_covers_every_block_once(lib, M, N, K, sms):
     plan = sk.gemm_plan(M, N, K, sms)
     assert plan.tiles == -(-N // 128) and plan.kblocks == -(-K // 64)
     assert plan.blocks == plan.tiles * plan.kblocks
-    assert plan.ctas == min(sms, plan.blocks)
-    assert plan.mma_n == (16 if M <= 16 else 32)
+    # One whole tile per CTA when the tiles fill at least 90 % of the SMs, else
+    # one CTA per SM (never more CTAs than weight blocks).
+    tiles = -(-N // 128)
+    want = tiles if tiles <= sms and 10 * tiles >= 9 * sms else min(sms, plan.blocks)
+    assert plan.ctas == want
+    if plan.ctas == tiles:
+        assert plan.split_tiles == 0
+    assert plan.mma_n == (16 if M <= 16 else (32 if M <= 32 else 64))
     assert plan.smem_bytes <= 232448
     seen = {}
     per_cta = []

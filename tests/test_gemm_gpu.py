@@ -34,7 +34,8 @@ def run_gemm(x, W):
 # K tails, every M class (MMA N = 16 and 32), tiles split across many CTAs.
 SMALL = [(1, 16, 64), (1, 1, 8), (2, 128, 8), (3, 200, 136), (4, 2048, 7168),
          (5, 384, 1000), (8, 1000, 520), (16, 640, 7168), (17, 256, 4096),
-         (24, 130, 200), (31, 257, 72), (32, 384, 7168), (32, 2048, 1024)]
+         (24, 130, 200), (31, 257, 72), (32, 384, 7168), (32, 2048, 1024),
+         (33, 300, 1000), (48, 1024, 7168), (64, 256, 14336), (64, 129, 72)]
 
 
 @pytest.mark.parametrize("M,N,K", SMALL)
@@ -44,7 +45,8 @@ def test_gemm_small_full_compare(cuda_ok, M, N, K):
     check_gemm_full(x, W, out)
 
 
-@pytest.mark.parametrize("M,N,K", [(32, 2048, 7168), (7, 1152, 18432), (1, 640, 7168)])
+@pytest.mark.parametrize("M,N,K", [(32, 2048, 7168), (7, 1152, 18432), (1, 640, 7168),
+                                   (64, 1024, 14336)])
 def test_gemm_integer_inputs_bit_exact(cuda_ok, M, N, K):
     """x, W in [-4, 4]: all partial sums are integers below 2^24, so any FP32
     order is exact and the GPU must equal the oracle bit for bit. Pins the tile,
@@ -64,7 +66,8 @@ def test_gemm_pr1(cuda_ok):
 
 FULL_SIZE = ([(m, n, 7168) for m in (1, 2, 4, 8, 16, 24, 32) for n in (4096, 12288, 18432)]
              + [(m, 20480, 7168) for m in (1, 8, 32)]
-             + [(16, 18432, 7168), (16, 7168, 18432)])
+             + [(16, 18432, 7168), (16, 7168, 18432)]
+             + [(m, 7168, 14336) for m in (16, 64)] + [(48, 18432, 7168), (64, 20480, 7168)])
 
 
 @pytest.mark.parametrize("M,N,K", FULL_SIZE)

@@ -1,0 +1,46 @@
+"""The decode GEMM's bounded waits on the GPU: a wait that can never complete ends
+with a recorded status instead of a hang, the kernel cleans up after itself
+(in-flight copies drained, tensor memory freed), and the context stays usable --
+the next regular call returns the right bits. Nothing here faults or traps."""
+import pytest
+import torch
+
+import skinny_bf16_gemm_gb300 as sk
+import workloads
+from gpu_helpers import gemm_inputs_device
+
+pytestmark = pytest.mark.gpu
+
+SELFTEST_BIT = 32  # the self-test's deliberate wait ran out
+
+
+def _gemm(x, W):
+    out = torch.empty(x.shape[0], W.shape[0], dtype=torch.bfloat16, device="cuda")
+    sk.decode_gemm_bf16(x, W, out)
+    torch.cuda.synchronize()
+    return out
+
+
+@pytest.mark.parametrize("M,N,K", [(4, 2048, 7168), (32, 18432, 7168)])
+def test_bounded_wait_reports_and_recovers(cuda_ok, M, N, K):
+    x, W = gemm_inputs_device(M, N, K, workloads.seed_for("watchdog", M, N, K))
+    ref = _gemm(x, W)
+    assert sk.device_error() == (0, 0)
+
+    junk = torch.empty_like(ref)
+    sk.watchdog_selftest(x, W, junk, timeout_ns=2_000_000)  # 2 ms limit
+    status, word = sk.device_error()
+    assert status == 9, sk.status_string(status)
+    assert word & SELFTEST_BIT
+
+    again = _gemm(x, W)
+    assert sk.device_error() == (0, 0)
+    assert torch.equal(again.view(torch.int16), ref.view(torch.int16))
+
+
+def test_selftest_rejects_out_of_range_limits(cuda_ok):
+    x, W = gemm_inputs_device(1, 16, 64, 3)
+    out = torch.empty(1, 16, dtype=torch.bfloat16, device="cuda")
+    for bad in (0, 999, 3_000_000_000):
+        with pytest.raises(sk.SkinnyError):
+            sk.watchdog_selftest(x, W, out, timeout_ns=bad)

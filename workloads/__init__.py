@@ -149,6 +149,11 @@ REDUCE_SWEEP = [ReduceShape(tp, m, res) for tp in (2, 4, 8) for m in (1, 4, 8, 1
 GEMM_SWEEP = [GemmShape(m, n, 7168) for m in (1, 2, 4, 8, 16, 24, 32)
               for n in (4096, 12288, 18432)]
 
+# Wider shapes beyond the pages' 32 rows: M up to 64 (the row cap) and the TP1
+# down projection's K = 14336 ("drafter/linears", warp_eligible).
+GEMM_WIDER = ([GemmShape(m, 18432, 7168) for m in (48, 64)] + [GemmShape(64, 20480, 7168)]
+              + [GemmShape(m, 7168, 14336) for m in (16, 32, 64)])
+
 # Vocab-shard lm_head GEMM.
 LM_HEAD = [GemmShape(m, 20480, 7168) for m in (1, 8, 32)]
 
