@@ -345,6 +345,19 @@ def run_sweep(args):
                         "frac_measured": nb / (t * 1e-3) / 1e9 / peak, "rotation_copies": copies})
         del parts, ress
         torch.cuda.empty_cache()
+    for TP, M, S in ([(8, m, 896) for m in (1, 16, 64)] + [(8, m, 2560) for m in (1, 8, 32, 64)]):
+        per = 2 * TP * M * S
+        copies = _rotation(per)
+        shards = [torch.randn(TP, M, S, device=dev).to(torch.bfloat16) for _ in range(copies)]
+        out = torch.empty(M, TP * S, device=dev, dtype=torch.bfloat16)
+        t = _time_calls(lambda i: sk.gather_shards_bf16(shards[i], out), args.sweep_calls, copies,
+                        stream)
+        nb = 2 * per  # read every shard once, write the gathered rows once
+        results.append({"kind": "gather", "set": "context" if S == 896 else "logits", "TP": TP,
+                        "M": M, "S": S, "us": t * 1e3, "GBps": nb / (t * 1e-3) / 1e9,
+                        "frac_measured": nb / (t * 1e-3) / 1e9 / peak, "rotation_copies": copies})
+        del shards
+        torch.cuda.empty_cache()
     print(json.dumps({"sweep": results, "peak_gbs": peak, "peak_source": peak_kind,
                       "pdl": bool(args.pdl), "calls_per_config": args.sweep_calls}), flush=True)
     return 0
@@ -457,7 +470,8 @@ def main():
 
     # ---- per-kernel durations: each kernel back to back on the same stream ----
     # The chain's own launch sequence with the reduce calls left out (and then
-    # the reduces alone), timed with CUDA events around the whole loop: the
+    # the reduces alone, replayed from a CUDA graph), timed with CUDA events
+    # around the whole loop: the
     # average launch duration of a kernel as it runs in a stream (programmatic
     # dependent launch on, as in the timed region). Events around every single
     # launch would serialise the kernels and add each launch's gap.
@@ -485,9 +499,31 @@ def main():
         torch.cuda.synchronize()
         return e0.elapsed_time(e1)
 
+    def graph_ms(fn, reps):
+        # A kernel of a few microseconds launched from Python is host-bound:
+        # capture the launches once and time the graph's replay instead.
+        fn()
+        torch.cuda.synchronize()
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(graph, stream=side):
+                for _ in range(reps):
+                    fn()
+        stream.wait_stream(side)
+        graph.replay()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        graph.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+
     gemm_launches = kernel_steps * 2 * cfg.layers
     gemm_ms = loop_ms(gemm_only, kernel_steps) / gemm_launches
-    reduce_ms = loop_ms(reduce_only, kernel_steps) / (kernel_steps * cfg.layers)
+    reduce_reps = 100
+    reduce_ms = graph_ms(reduce_only, reduce_reps) / (reduce_reps * cfg.layers)
     g1 = cfg.gemm1()
     gemm_bytes = g1.algorithmic_bytes()  # GEMM1 and GEMM2 move the same bytes
     peak, peak_kind = measured_peaks()

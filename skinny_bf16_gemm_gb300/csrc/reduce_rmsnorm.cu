@@ -14,8 +14,7 @@
 // the warps in order, then the C CTA sums exchanged through distributed shared
 // memory and added in CTA order (every CTA gets the same bits).
 // With programmatic dependent launch, gamma (a weight) is loaded before waiting
-// for the previous kernel; the partial rows and the residual after, and the
-// next kernel is released once the wait is over.
+// for the previous kernel; the partial rows and the residual after.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -79,10 +78,10 @@ __global__ void __launch_bounds__(ReduceShape<C>::kThreads)
 
     uint4 gw = make_uint4(0, 0, 0, 0);
     if (active) gw = __ldg(gamma + frag);
-    ptx::pdl_wait();  // the partial rows may be the previous kernel's output
-    // Only now let the next kernel launch: a decode GEMM that follows streams its
-    // weights while this short kernel runs, rather than long before.
+    // The next kernel may launch now: a decode GEMM that follows sets up and
+    // streams its first weights while this kernel waits and runs.
     ptx::pdl_launch_dependents();
+    ptx::pdl_wait();  // the partial rows may be the previous kernel's output
 
     float h[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     float ss = 0.0f;
