@@ -27,7 +27,7 @@
  *    kernel whose internal wait ran out instead records a code that
  *    skinny_device_error() returns.
  *  - Nothing is allocated per call. decode_gemm_bf16 uses a per-device scratch
- *    area (split-K partial sums, tile counters, an error word) that its first
+ *    area (split-K partial sums, published-partial flags, an error word) that its first
  *    call on each device allocates with cudaMalloc; make that first call outside
  *    CUDA stream capture. Calls on one device whose kernels may overlap in time
  *    (unordered streams) share that scratch and must not be issued.
@@ -128,14 +128,14 @@ SKINNY_API int decode_gemm_bf16_logits(const void *x, const void *W, void *out, 
  *   implicit synchronisation.
  *
  *   Same arguments, layouts, results and errors as decode_gemm_bf16 (the same
- *   kernel runs). The split-K scratch -- partial tiles, tile counters, error
+ *   kernel runs). The split-K scratch -- partial tiles, published-partial flags, error
  *   word -- lives instead in one static device array of the library, 5.2 MB,
  *   which every GPU that loads the library holds until the process exits. It has
  *   partial-tile slots for 160 CTAs of up to 32 rows: the call runs with
  *   min(SM count, 160) CTAs and rejects M > 32 with SKINNY_ERR_SHAPE.
  *   The first call on each device looks up the array's device address
  *   (cudaGetSymbolAddress); make that first call before any stream capture.
- *   Each call first clears the counters and the error word with a
+ *   Each call first clears the flags and the error word with a
  *   cudaMemsetAsync on `stream`, then launches the kernel. All calls share the
  *   one array: calls whose GPU work may overlap (streams not ordered with each
  *   other on the same device) race and give wrong results; order them. A kernel
@@ -206,7 +206,7 @@ SKINNY_API const char *skinny_status_string(int status);
  *   Synchronises the device, then returns SKINNY_OK if no kernel of this library
  *   recorded a problem since the last read, else SKINNY_ERR_TIMEOUT, and writes
  *   the raw word (a bit set per waiting role that gave up) to *word if word is
- *   not NULL. Clearing also re-arms the decode GEMM's scratch counters, so the
+ *   not NULL. Clearing also re-arms the decode GEMM's scratch flags, so the
  *   next call starts clean. Host pointer: word.
  */
 SKINNY_API int skinny_device_error(int device, int *word);

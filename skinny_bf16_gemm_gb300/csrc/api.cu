@@ -26,9 +26,9 @@ struct DeviceState {
     // Split-K scratch of the decode GEMM, sized for one CTA per SM.
     void *scratch = nullptr;
     float *partials = nullptr;
-    unsigned *counters = nullptr;
+    unsigned *flags = nullptr;
     int *err = nullptr;
-    size_t counter_bytes = 0;
+    size_t flag_bytes = 0;
 };
 
 std::mutex g_mutex;
@@ -86,8 +86,8 @@ int ensure_scratch(int dev, cudaStream_t stream, DeviceState **out) {
         }
         if (cap != cudaStreamCaptureStatusNone) return SKINNY_ERR_CAPTURE;
         const size_t partial_bytes = static_cast<size_t>(2) * d->sms * kSlotFloats * sizeof(float);
-        const size_t counter_bytes = (static_cast<size_t>(d->sms) * sizeof(unsigned) + 255) / 256 * 256;
-        const size_t bytes = partial_bytes + counter_bytes + 256;
+        const size_t flag_bytes = (static_cast<size_t>(2) * d->sms * sizeof(unsigned) + 255) / 256 * 256;
+        const size_t bytes = partial_bytes + flag_bytes + 256;
         void *p = nullptr;
         if (cudaMalloc(&p, bytes) != cudaSuccess) {
             cudaGetLastError();
@@ -100,9 +100,9 @@ int ensure_scratch(int dev, cudaStream_t stream, DeviceState **out) {
         }
         d->scratch = p;
         d->partials = static_cast<float *>(p);
-        d->counters = reinterpret_cast<unsigned *>(static_cast<char *>(p) + partial_bytes);
-        d->err = reinterpret_cast<int *>(static_cast<char *>(p) + partial_bytes + counter_bytes);
-        d->counter_bytes = counter_bytes;
+        d->flags = reinterpret_cast<unsigned *>(static_cast<char *>(p) + partial_bytes);
+        d->err = reinterpret_cast<int *>(static_cast<char *>(p) + partial_bytes + flag_bytes);
+        d->flag_bytes = flag_bytes;
     }
     *out = d;
     return SKINNY_OK;
@@ -197,7 +197,7 @@ int gemm_launch(const void *x, const void *W, void *out, int M, int N, int K, vo
     a.out = static_cast<uint16_t *>(out);
     a.partials = d->partials;
     a.slot_floats = kSlotFloats;
-    a.counters = d->counters;
+    a.flags = d->flags;
     a.err = d->err;
     a.wait_limit_ns = limit_ns;
     a.selftest = selftest;
@@ -251,9 +251,9 @@ int gemm_launch_static(const void *x, const void *W, void *out, int M, int N, in
     const int ctas = choose_ctas(N, d->sms);
     const GemmGeometry g = make_geometry(M, N, K, ctas < sc.max_ctas ? ctas : sc.max_ctas);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // The array keeps the previous call's contents: the tile counters and the
-    // error word must start this call at zero.
-    if (cudaMemsetAsync(sc.counters, 0, sc.zero_bytes, s) != cudaSuccess) {
+    // The array keeps the previous call's contents: the published-partial flags
+    // and the error word must start this call at zero.
+    if (cudaMemsetAsync(sc.flags, 0, sc.zero_bytes, s) != cudaSuccess) {
         cudaGetLastError();
         return SKINNY_ERR_LAUNCH;
     }
@@ -264,7 +264,7 @@ int gemm_launch_static(const void *x, const void *W, void *out, int M, int N, in
     a.out = static_cast<uint16_t *>(out);
     a.partials = sc.partials;
     a.slot_floats = kStaticSlotRows * kBlockN;
-    a.counters = sc.counters;
+    a.flags = sc.flags;
     a.err = sc.err;
     a.wait_limit_ns = kWaitLimitNs;
     a.selftest = 0;
@@ -427,9 +427,9 @@ int skinny_device_error(int device, int *word) {
                 cudaGetLastError();
                 st = SKINNY_ERR_DEVICE;
             } else if (value != 0) {
-                // A kernel gave up part-way: clear the word and the tile counters.
+                // A kernel gave up part-way: clear the word and the partial flags.
                 if (cudaMemset(d.err, 0, sizeof(int)) != cudaSuccess ||
-                    cudaMemset(d.counters, 0, d.counter_bytes) != cudaSuccess) {
+                    cudaMemset(d.flags, 0, d.flag_bytes) != cudaSuccess) {
                     cudaGetLastError();
                     st = SKINNY_ERR_DEVICE;
                 }

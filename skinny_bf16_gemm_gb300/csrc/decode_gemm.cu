@@ -12,10 +12,13 @@
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator (TMEM lane = weight row =
 //               output column n, column = output row m), one BF16 rounding, or
 //               the split-K fix-up.
-// Work split (plan.cuh): the ceil(N/128) x ceil(K/64) weight blocks are dealt to
-// the CTAs as equal contiguous ranges. A tile whose K range is shared by several
-// CTAs is finished by the last to arrive (an atomic counter per tile), which adds
-// all FP32 partial sums in K order, so results do not depend on arrival order.
+// Work split (plan.cuh): one whole 128-row tile per CTA when the tiles nearly fill
+// the GPU, otherwise the ceil(N/128) x ceil(K/64) weight blocks dealt to one CTA
+// per SM as equal contiguous ranges (stream-K). A tile whose K range is shared
+// by several CTAs is finished by the CTA holding its first K blocks (for which it
+// is the last piece): the others publish their FP32 partials behind a release
+// flag, and the finisher adds them in K order, so the bits do not depend on
+// timing.
 // Before waiting on the previous kernel in the stream (programmatic dependent
 // launch) the producer already streams the first STAGES weight tiles: weights
 // never depend on the previous kernel, x may.
@@ -298,58 +301,57 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t fix_phase = 0;
         bool fix_pending = false;
 
-        // Finish shared tile t: add the FP32 partial sums of CTAs first..last in K
-        // (= CTA) order and round once. Partials are pulled into the ring (free
-        // by then) with bulk copies, all in flight at once. own != nullptr: this
-        // CTA's partial is in registers and is not copied. false = aborted.
+        // Finish split tile t. This CTA holds the tile's first K blocks, so the
+        // tile is its last piece: its own partial is in registers and the ring
+        // is free. Wait until the other contributors have published their
+        // partials, pull them into the ring with bulk copies (all in flight at
+        // once), add in K (= CTA) order and round once. false = aborted.
         auto finish_tile = [&](int t, int first, int last, const float *own) -> bool {
             float sum[MP];
 #pragma unroll
-            for (int m = 0; m < MP; ++m) sum[m] = 0.0f;
-            bool started = false;
-            int c0 = first;
-            while (c0 <= last) {
-                // The next chunk of contributors whose copies fit in the ring.
-                int c1 = c0, copies = 0;
-                while (c1 <= last && (copies < ring_slots || (own && c1 == cta))) {
-                    if (!(own && c1 == cta)) ++copies;
-                    ++c1;
-                }
-                if (copies > 0) {
-                    if (etid == 0) {
-                        __threadfence();
-                        ptx::fence_proxy_async_global();
-                        ptx::mbar_arrive_expect_tx(bar_fix, static_cast<uint32_t>(copies * slot_bytes));
-                        int i = 0;
-                        for (int c = c0; c < c1; ++c) {
-                            if (own && c == cta) continue;
-                            ptx::bulk_load(sbase + i * slot_bytes,
-                                           args.partials + static_cast<size_t>(partial_slot(g, c, t)) * args.slot_floats,
-                                           slot_bytes, bar_fix);
-                            ++i;
+            for (int m = 0; m < MP; ++m) sum[m] = own[m];
+            for (int c0 = first + 1; c0 <= last;) {
+                const int c1 = last + 1 < c0 + ring_slots ? last + 1 : c0 + ring_slots;
+                const int n_in = c1 - c0;
+                // One thread per contributor of this chunk waits for its flag.
+                int r = kWaitDone;
+                if (etid < n_in) {
+                    const unsigned *flag = args.flags + partial_slot(g, c0 + etid, t);
+                    if (ptx::ld_relaxed_gpu(flag) == 0u) {
+                        const uint64_t t0 = ptx::global_timer_ns();
+                        for (uint32_t spin = 1; ptx::ld_relaxed_gpu(flag) == 0u; ++spin) {
+                            if ((spin & 15u) == 0) {
+                                if (*abort_flag) { r = kWaitAborted; break; }
+                                if (ptx::global_timer_ns() - t0 > limit) { r = kWaitTimeout; break; }
+                            }
                         }
                     }
-                    fix_pending = true;
-                    const int r = bounded_wait(bar_fix, fix_phase, abort_flag, limit);
-                    if (r == kWaitTimeout) raise_error(args.err, abort_flag, kErrEpilogueWait);
-                    if (epilogue_any(r != kWaitDone)) return false;
-                    fix_pending = false;
-                    fix_phase ^= 1u;
+                    __threadfence();  // acquire: the partial behind the flag is visible
                 }
-                int i = 0;
+                if (r == kWaitTimeout) raise_error(args.err, abort_flag, kErrEpilogueWait);
+                if (epilogue_any(r != kWaitDone)) return false;
+                if (etid == 0) {
+                    ptx::fence_proxy_async_global();
+                    ptx::mbar_arrive_expect_tx(bar_fix, static_cast<uint32_t>(n_in * slot_bytes));
+                    for (int c = c0; c < c1; ++c)
+                        ptx::bulk_load(sbase + (c - c0) * slot_bytes,
+                                       args.partials + static_cast<size_t>(partial_slot(g, c, t)) * args.slot_floats,
+                                       slot_bytes, bar_fix);
+                }
+                fix_pending = true;
+                r = bounded_wait(bar_fix, fix_phase, abort_flag, limit);
+                if (r == kWaitTimeout) raise_error(args.err, abort_flag, kErrEpilogueWait);
+                if (epilogue_any(r != kWaitDone)) return false;
+                fix_pending = false;
+                fix_phase ^= 1u;
                 for (int c = c0; c < c1; ++c) {
-                    const bool mine = own && c == cta;
-                    const float *src = staging + static_cast<size_t>(i) * g.M * kBlockN + row;
+                    const float *src = staging + static_cast<size_t>(c - c0) * g.M * kBlockN + row;
 #pragma unroll
-                    for (int m = 0; m < MP; ++m) {
-                        if (m < g.M) {
-                            const float v = mine ? own[m] : src[m * kBlockN];
-                            sum[m] = started ? __fadd_rn(sum[m], v) : v;
-                        }
-                    }
-                    started = true;
-                    if (!mine) ++i;
+                    for (int m = 0; m < MP; ++m)
+                        if (m < g.M) sum[m] = __fadd_rn(sum[m], src[m * kBlockN]);
                 }
+                // The partials are consumed: re-arm their flags for the next call.
+                if (etid < n_in) args.flags[partial_slot(g, c0 + etid, t)] = 0u;
                 ptx::named_barrier_sync(1, kEpilogueThreads);  // the ring is refilled next
                 c0 = c1;
             }
@@ -363,22 +365,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             return true;
         };
 
-        // Shared tiles this CTA arrived last at while streaming: tile, first and
-        // last contributor (register-resident; at most two -- only a range's first
-        // and last pieces can be partial). They are finished once the ring is free.
-        int4 fin[2] = {make_int4(0, 0, 0, 0), make_int4(0, 0, 0, 0)};
-        int fin_count = 0;
-        bool aborted = false;
         for (int q = 0; q < pieces; ++q) {
             const Piece p = cta_piece(g, cta, q);
             const int b = q & 1;
             const uint32_t aph = (q >> 1) & 1;
             const int r = bounded_wait(bar_acc_full + 8 * b, aph, abort_flag, limit);
             if (r == kWaitTimeout) raise_error(args.err, abort_flag, kErrEpilogueWait);
-            if (epilogue_any(r != kWaitDone)) {
-                aborted = true;
-                break;
-            }
+            if (epilogue_any(r != kWaitDone)) break;
             ptx::tc_fence_after_sync();
             float acc[MP];
             {
@@ -410,56 +403,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             int first, last;
             tile_contributors(g, p.tile, first, last);
-            if (q == pieces - 1) {
-                // This CTA's last piece: the ring is free. If every other
-                // contributor has arrived already -- the usual case, they covered
-                // this tile at the start of their ranges -- finish the tile now
-                // from their partials and this CTA's registers.
-                if (etid == 0) {
-                    const unsigned others = static_cast<unsigned>(last - first);
-                    const bool all_in = ptx::ld_acquire_gpu(args.counters + first) == others;
-                    if (all_in) args.counters[first] = 0u;  // re-armed for the next call
-                    misc[2] = all_in ? 1u : 0u;
-                }
-                ptx::named_barrier_sync(1, kEpilogueThreads);
-                const bool direct = misc[2] != 0u;
-                ptx::named_barrier_sync(1, kEpilogueThreads);  // misc[2] is reused below
-                if (direct) {
-                    if (!finish_tile(p.tile, first, last, acc)) {
-                        aborted = true;
-                        break;
-                    }
-                    continue;
-                }
+            if (first == cta) {
+                // The tile starts in this CTA's range: this CTA finishes it.
+                if (!finish_tile(p.tile, first, last, acc)) break;
+                continue;
             }
-            // Publish this CTA's partial and count the arrival; the CTA that
-            // arrives last finishes the tile once its own pieces are done.
+            // Publish this CTA's partial: the values, then a release flag. The
+            // finishing CTA reads them with bulk copies (the async proxy).
             float *mine =
                 args.partials + static_cast<size_t>(partial_slot(g, cta, p.tile)) * args.slot_floats;
 #pragma unroll
             for (int m = 0; m < MP; ++m)
                 if (m < g.M) __stcg(mine + m * kBlockN + row, acc[m]);
-            ptx::fence_proxy_async_global();  // the finishing CTA reads it with bulk copies
+            ptx::fence_proxy_async_global();
             __threadfence();
             ptx::named_barrier_sync(1, kEpilogueThreads);
-            if (etid == 0) {
-                __threadfence();
-                const unsigned prev = atomicInc(args.counters + first, static_cast<unsigned>(last - first));
-                misc[2] = prev == static_cast<unsigned>(last - first) ? 1u : 0u;
-                __threadfence();
-            }
-            ptx::named_barrier_sync(1, kEpilogueThreads);
-            if (misc[2] != 0u) {
-                const int4 rec = make_int4(p.tile, first, last, 0);
-                if (fin_count == 0) fin[0] = rec;
-                else fin[1] = rec;
-                fin_count = fin_count < 2 ? fin_count + 1 : 2;
-            }
-            ptx::named_barrier_sync(1, kEpilogueThreads);  // misc[2] is reused next piece
-        }
-        for (int f = 0; f < fin_count && !aborted; ++f) {
-            const int4 rec = f == 0 ? fin[0] : fin[1];
-            if (!finish_tile(rec.x, rec.y, rec.z, nullptr)) aborted = true;
+            if (etid == 0) ptx::st_release_gpu(args.flags + partial_slot(g, cta, p.tile), 1u);
         }
         if (fix_pending) {
             // Copies still in flight must land before the CTA's memory is released.
@@ -577,7 +536,7 @@ cudaError_t launch_decode_gemm(const CUtensorMap &w_map, const CUtensorMap &x_ma
 //
 // The same kernel can run with its split-K scratch in this file-scope array
 // instead of memory from cudaMalloc. Sized for kStaticScratchCtas CTAs with
-// partial tiles of up to 32 rows: 2 slots per CTA, then one counter per CTA, then
+// partial tiles of up to 32 rows: 2 slots per CTA, then one flag per slot, then
 // the error word. Every GPU that loads the library holds it until the process
 // exits.
 namespace skinny {
@@ -585,9 +544,9 @@ namespace {
 
 constexpr size_t kStaticPartialBytes =
     static_cast<size_t>(2) * kStaticScratchCtas * kStaticSlotRows * kBlockN * sizeof(float);
-constexpr size_t kStaticCounterBytes = 1024;  // >= kStaticScratchCtas counters, 256-aligned
-constexpr size_t kStaticScratchBytes = kStaticPartialBytes + kStaticCounterBytes + 256;
-static_assert(kStaticScratchCtas * sizeof(unsigned) <= kStaticCounterBytes, "counter space");
+constexpr size_t kStaticFlagBytes = 2048;  // >= 2 * kStaticScratchCtas flags, 256-aligned
+constexpr size_t kStaticScratchBytes = kStaticPartialBytes + kStaticFlagBytes + 256;
+static_assert(2 * kStaticScratchCtas * sizeof(unsigned) <= kStaticFlagBytes, "flag space");
 
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
@@ -613,9 +572,9 @@ cudaError_t static_scratch_for_current_device(StaticScratch *out) {
     }
     char *base = static_cast<char *>(g_static_base[dev]);
     out->partials = reinterpret_cast<float *>(base);
-    out->counters = reinterpret_cast<unsigned *>(base + kStaticPartialBytes);
-    out->err = reinterpret_cast<int *>(base + kStaticPartialBytes + kStaticCounterBytes);
-    out->zero_bytes = kStaticCounterBytes + sizeof(int);  // counters and error word
+    out->flags = reinterpret_cast<unsigned *>(base + kStaticPartialBytes);
+    out->err = reinterpret_cast<int *>(base + kStaticPartialBytes + kStaticFlagBytes);
+    out->zero_bytes = kStaticFlagBytes + sizeof(int);  // flags and error word
     out->max_ctas = kStaticScratchCtas;
     return cudaSuccess;
 }

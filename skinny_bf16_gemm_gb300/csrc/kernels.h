@@ -22,7 +22,7 @@ struct GemmArgs {
     uint16_t *out;          // [M, N] BF16 patterns
     float *partials;        // [2 * ctas][slot rows][128] FP32 split-K partial tiles
     int slot_floats;        // floats from one partial tile to the next
-    unsigned *counters;     // [ctas] arrival counters, zero between calls
+    unsigned *flags;        // [2 * ctas] "partial published" flags, zero between calls
     int *err;               // device error word
     unsigned long long wait_limit_ns;
     int selftest;           // 1: the MMA role waits on a barrier nothing completes
@@ -48,9 +48,9 @@ constexpr int kStaticSlotRows = 32;       // rows of x a static partial tile hol
 
 struct StaticScratch {
     float *partials;      // [2 * max_ctas][kStaticSlotRows][128] FP32
-    unsigned *counters;   // [max_ctas], contiguous with err
-    int *err;             // error word, right after the counter space
-    size_t zero_bytes;    // bytes from `counters` through `err` that must start at zero
+    unsigned *flags;      // [2 * max_ctas], contiguous with err
+    int *err;             // error word, right after the flag space
+    size_t zero_bytes;    // bytes from `flags` through `err` that must start at zero
     int max_ctas;
 };
 
