@@ -313,10 +313,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c0 = first + 1; c0 <= last;) {
                 const int c1 = last + 1 < c0 + ring_slots ? last + 1 : c0 + ring_slots;
                 const int n_in = c1 - c0;
-                // One thread per contributor of this chunk waits for its flag.
+                // The barrier expects every copy of this chunk; one thread per
+                // contributor waits for its flag and starts its copy at once, so
+                // early partials are on their way while late ones are published.
+                if (etid == 0)
+                    ptx::mbar_arrive_expect_tx(bar_fix, static_cast<uint32_t>(n_in * slot_bytes));
+                fix_pending = true;
                 int r = kWaitDone;
                 if (etid < n_in) {
-                    const unsigned *flag = args.flags + partial_slot(g, c0 + etid, t);
+                    const int c = c0 + etid;
+                    const unsigned *flag = args.flags + partial_slot(g, c, t);
                     if (ptx::ld_relaxed_gpu(flag) == 0u) {
                         const uint64_t t0 = ptx::global_timer_ns();
                         for (uint32_t spin = 1; ptx::ld_relaxed_gpu(flag) == 0u; ++spin) {
@@ -326,19 +332,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                             }
                         }
                     }
-                    __threadfence();  // acquire: the partial behind the flag is visible
+                    if (r == kWaitDone) {
+                        __threadfence();                  // acquire the partial behind the flag
+                        ptx::fence_proxy_async_global();  // ... for the bulk copy that reads it
+                        ptx::bulk_load(sbase + etid * slot_bytes,
+                                       args.partials + static_cast<size_t>(partial_slot(g, c, t)) * args.slot_floats,
+                                       slot_bytes, bar_fix);
+                    }
                 }
                 if (r == kWaitTimeout) raise_error(args.err, abort_flag, kErrEpilogueWait);
                 if (epilogue_any(r != kWaitDone)) return false;
-                if (etid == 0) {
-                    ptx::fence_proxy_async_global();
-                    ptx::mbar_arrive_expect_tx(bar_fix, static_cast<uint32_t>(n_in * slot_bytes));
-                    for (int c = c0; c < c1; ++c)
-                        ptx::bulk_load(sbase + (c - c0) * slot_bytes,
-                                       args.partials + static_cast<size_t>(partial_slot(g, c, t)) * args.slot_floats,
-                                       slot_bytes, bar_fix);
-                }
-                fix_pending = true;
                 r = bounded_wait(bar_fix, fix_phase, abort_flag, limit);
                 if (r == kWaitTimeout) raise_error(args.err, abort_flag, kErrEpilogueWait);
                 if (epilogue_any(r != kWaitDone)) return false;
@@ -416,9 +419,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int m = 0; m < MP; ++m)
                 if (m < g.M) __stcg(mine + m * kBlockN + row, acc[m]);
             ptx::fence_proxy_async_global();
-            __threadfence();
             ptx::named_barrier_sync(1, kEpilogueThreads);
-            if (etid == 0) ptx::st_release_gpu(args.flags + partial_slot(g, cta, p.tile), 1u);
+            // One release (fence + store) after the barrier covers every thread's
+            // stores of the partial.
+            if (etid == 0) {
+                __threadfence();
+                ptx::st_release_gpu(args.flags + partial_slot(g, cta, p.tile), 1u);
+            }
         }
         if (fix_pending) {
             // Copies still in flight must land before the CTA's memory is released.
@@ -495,7 +502,8 @@ cudaError_t launch_variant(const CUtensorMap &w_map, const CUtensorMap &x_map,
 }
 
 constexpr int kDeepStages16 = 10, kDeepStages32 = 9, kDeepStages64 = 7;
-constexpr int kShallowStages = 5, kShallowStages64 = 4;
+// Shallow rings sized so two CTAs fit on one SM (about 112, 104 and 100 KB).
+constexpr int kShallowStages16 = 6, kShallowStages32 = 5, kShallowStages64 = 4;
 
 }  // namespace
 
@@ -503,15 +511,15 @@ constexpr int kShallowStages = 5, kShallowStages64 = 4;
 // overlap on each SM); the deep ring otherwise.
 int gemm_stages(int mma_n, bool pdl) {
     if (mma_n == 64) return pdl ? kShallowStages64 : kDeepStages64;
-    if (pdl) return kShallowStages;
+    if (pdl) return mma_n == 16 ? kShallowStages16 : kShallowStages32;
     return mma_n == 16 ? kDeepStages16 : kDeepStages32;
 }
 
 int gemm_smem_bytes(int mma_n, bool pdl) {
     if (mma_n == 16)
-        return pdl ? Layout<16, kShallowStages>::kDynamicBytes : Layout<16, kDeepStages16>::kDynamicBytes;
+        return pdl ? Layout<16, kShallowStages16>::kDynamicBytes : Layout<16, kDeepStages16>::kDynamicBytes;
     if (mma_n == 32)
-        return pdl ? Layout<32, kShallowStages>::kDynamicBytes : Layout<32, kDeepStages32>::kDynamicBytes;
+        return pdl ? Layout<32, kShallowStages32>::kDynamicBytes : Layout<32, kDeepStages32>::kDynamicBytes;
     return pdl ? Layout<64, kShallowStages64>::kDynamicBytes : Layout<64, kDeepStages64>::kDynamicBytes;
 }
 
@@ -519,11 +527,11 @@ cudaError_t launch_decode_gemm(const CUtensorMap &w_map, const CUtensorMap &x_ma
                                const GemmArgs &args, int mma_n, int ctas, cudaStream_t stream,
                                bool pdl, int device) {
     if (mma_n == 16) {
-        if (pdl) return launch_variant<16, kShallowStages>(w_map, x_map, args, ctas, stream, pdl, device);
+        if (pdl) return launch_variant<16, kShallowStages16>(w_map, x_map, args, ctas, stream, pdl, device);
         return launch_variant<16, kDeepStages16>(w_map, x_map, args, ctas, stream, pdl, device);
     }
     if (mma_n == 32) {
-        if (pdl) return launch_variant<32, kShallowStages>(w_map, x_map, args, ctas, stream, pdl, device);
+        if (pdl) return launch_variant<32, kShallowStages32>(w_map, x_map, args, ctas, stream, pdl, device);
         return launch_variant<32, kDeepStages32>(w_map, x_map, args, ctas, stream, pdl, device);
     }
     if (pdl) return launch_variant<64, kShallowStages64>(w_map, x_map, args, ctas, stream, pdl, device);
