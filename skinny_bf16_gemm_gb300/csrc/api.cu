@@ -209,7 +209,8 @@ int gemm_launch(const void *x, const void *W, void *out, int M, int N, int K, vo
         std::lock_guard<std::mutex> lock(g_mutex);
         pdl = g_pdl;
     }
-    cudaError_t e = launch_decode_gemm(w_map, x_map, a, mma_n, g.ctas, s, pdl, dev);
+    cudaError_t e = launch_decode_gemm(w_map, x_map, a, mma_n, g.ctas, s, pdl,
+                                       use_shallow_ring(g, pdl), dev);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return SKINNY_ERR_LAUNCH;
@@ -276,7 +277,8 @@ int gemm_launch_static(const void *x, const void *W, void *out, int M, int N, in
         std::lock_guard<std::mutex> lock(g_mutex);
         pdl = g_pdl;
     }
-    cudaError_t e = launch_decode_gemm(w_map, x_map, a, mma_n, g.ctas, s, pdl, dev);
+    cudaError_t e = launch_decode_gemm(w_map, x_map, a, mma_n, g.ctas, s, pdl,
+                                       use_shallow_ring(g, pdl), dev);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return SKINNY_ERR_LAUNCH;
@@ -465,8 +467,8 @@ int skinny_gemm_plan_query(int M, int N, int K, int num_sms, skinny_gemm_plan *p
         std::lock_guard<std::mutex> lock(g_mutex);
         pdl = g_pdl;
     }
-    plan->stages = gemm_stages(plan->mma_n, pdl);
-    plan->smem_bytes = gemm_smem_bytes(plan->mma_n, pdl);
+    plan->stages = gemm_stages(plan->mma_n, use_shallow_ring(g, pdl));
+    plan->smem_bytes = gemm_smem_bytes(plan->mma_n, use_shallow_ring(g, pdl));
     int split = 0;
     for (int t = 0; t < g.tiles; ++t) {
         int first, last;

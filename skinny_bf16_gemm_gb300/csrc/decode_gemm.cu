@@ -45,9 +45,10 @@ constexpr uint64_t kDrainLimitNs = 200000000ull;  // 0.2 s for copies already is
 constexpr int kL2PrefetchBlocks = 6;  // weight blocks prefetched to L2 before the ring's
 
 // MP: padded row count (MMA N). STAGES: shared-memory ring depth. The deep ring
-// (~185 KB) keeps the most bytes in flight; the shallow one (~92-101 KB) lets the
-// next kernel's CTAs be resident on the same SM while this one finishes, so
-// with programmatic dependent launch they stream weights across the boundary.
+// (~185 KB) keeps the most bytes in flight; the shallow one (~100-112 KB) lets
+// the next kernel's CTAs be resident on the same SM while this one finishes, so
+// with programmatic dependent launch they stream weights across the boundary
+// (plan.cuh use_shallow_ring picks one by the weight bytes per CTA).
 template <int MP, int STAGES>
 struct Layout {
     static constexpr int kStages = STAGES;
@@ -165,9 +166,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem_base = misc[0];
     volatile uint32_t *abort_flag = misc + 1;
 
-    // The next kernel in the stream may launch now: its CTAs fit beside this one
-    // (shallow ring), set up and stream their first weights while this grid
-    // runs, and wait for it before touching anything it writes.
+    // The next kernel in the stream may launch now: its CTAs take SMs as they
+    // free up (beside this one with the shallow ring), set up and stream their
+    // first weights while this grid runs, and wait for it before touching
+    // anything it writes.
     ptx::pdl_launch_dependents();
 
     const int pieces = cta_piece_count(g, cta);
@@ -507,34 +509,32 @@ constexpr int kShallowStages16 = 6, kShallowStages32 = 5, kShallowStages64 = 4;
 
 }  // namespace
 
-// The shallow ring goes with programmatic dependent launch (consecutive kernels
-// overlap on each SM); the deep ring otherwise.
-int gemm_stages(int mma_n, bool pdl) {
-    if (mma_n == 64) return pdl ? kShallowStages64 : kDeepStages64;
-    if (pdl) return mma_n == 16 ? kShallowStages16 : kShallowStages32;
+int gemm_stages(int mma_n, bool shallow) {
+    if (mma_n == 64) return shallow ? kShallowStages64 : kDeepStages64;
+    if (shallow) return mma_n == 16 ? kShallowStages16 : kShallowStages32;
     return mma_n == 16 ? kDeepStages16 : kDeepStages32;
 }
 
-int gemm_smem_bytes(int mma_n, bool pdl) {
+int gemm_smem_bytes(int mma_n, bool shallow) {
     if (mma_n == 16)
-        return pdl ? Layout<16, kShallowStages16>::kDynamicBytes : Layout<16, kDeepStages16>::kDynamicBytes;
+        return shallow ? Layout<16, kShallowStages16>::kDynamicBytes : Layout<16, kDeepStages16>::kDynamicBytes;
     if (mma_n == 32)
-        return pdl ? Layout<32, kShallowStages32>::kDynamicBytes : Layout<32, kDeepStages32>::kDynamicBytes;
-    return pdl ? Layout<64, kShallowStages64>::kDynamicBytes : Layout<64, kDeepStages64>::kDynamicBytes;
+        return shallow ? Layout<32, kShallowStages32>::kDynamicBytes : Layout<32, kDeepStages32>::kDynamicBytes;
+    return shallow ? Layout<64, kShallowStages64>::kDynamicBytes : Layout<64, kDeepStages64>::kDynamicBytes;
 }
 
 cudaError_t launch_decode_gemm(const CUtensorMap &w_map, const CUtensorMap &x_map,
                                const GemmArgs &args, int mma_n, int ctas, cudaStream_t stream,
-                               bool pdl, int device) {
+                               bool pdl, bool shallow, int device) {
     if (mma_n == 16) {
-        if (pdl) return launch_variant<16, kShallowStages16>(w_map, x_map, args, ctas, stream, pdl, device);
+        if (shallow) return launch_variant<16, kShallowStages16>(w_map, x_map, args, ctas, stream, pdl, device);
         return launch_variant<16, kDeepStages16>(w_map, x_map, args, ctas, stream, pdl, device);
     }
     if (mma_n == 32) {
-        if (pdl) return launch_variant<32, kShallowStages32>(w_map, x_map, args, ctas, stream, pdl, device);
+        if (shallow) return launch_variant<32, kShallowStages32>(w_map, x_map, args, ctas, stream, pdl, device);
         return launch_variant<32, kDeepStages32>(w_map, x_map, args, ctas, stream, pdl, device);
     }
-    if (pdl) return launch_variant<64, kShallowStages64>(w_map, x_map, args, ctas, stream, pdl, device);
+    if (shallow) return launch_variant<64, kShallowStages64>(w_map, x_map, args, ctas, stream, pdl, device);
     return launch_variant<64, kDeepStages64>(w_map, x_map, args, ctas, stream, pdl, device);
 }
 

@@ -33,14 +33,15 @@ struct GemmArgs {
 };
 
 // Pipeline depth and shared memory of the decode GEMM for a padded row count,
-// with or without programmatic dependent launch.
-int gemm_stages(int mma_n, bool pdl);
-int gemm_smem_bytes(int mma_n, bool pdl);
+// with the shallow or the deep ring (plan.cuh use_shallow_ring).
+int gemm_stages(int mma_n, bool shallow);
+int gemm_smem_bytes(int mma_n, bool shallow);
 
-// Launch the decode GEMM: grid = ctas CTAs of 192 threads.
+// Launch the decode GEMM: grid = ctas CTAs of 192 threads; pdl sets the
+// programmatic-dependent-launch attribute, shallow picks the ring.
 cudaError_t launch_decode_gemm(const CUtensorMap &w_map, const CUtensorMap &x_map,
                                const GemmArgs &args, int mma_n, int ctas, cudaStream_t stream,
-                               bool pdl, int device);
+                               bool pdl, bool shallow, int device);
 
 // Split-K scratch held in a static device array (decode_gemm_bf16_noalloc).
 constexpr int kStaticScratchCtas = 160;   // CTAs the array holds partial tiles for

@@ -48,6 +48,18 @@ __host__ __device__ inline int choose_ctas(int N, int num_sms) {
     return num_sms;
 }
 
+// Ring depth. A deep ring (one CTA per SM) keeps the most weight bytes in flight
+// and wins on long streams; a shallow one lets the next kernel's CTA share the
+// SM under programmatic dependent launch, which wins when each CTA streams
+// little (the next kernel's set-up and first weights then matter more). Measured
+// on GB300 the two cross near 1 MiB of weights per CTA.
+constexpr long long kShallowRingMaxBytes = 1ll << 20;
+
+__host__ __device__ inline bool use_shallow_ring(const GemmGeometry &g, bool pdl) {
+    const long long per_cta = g.blocks * (kBlockN * kBlockK * 2) / g.ctas;
+    return pdl && per_cta < kShallowRingMaxBytes;
+}
+
 // First weight block of CTA c (c = ctas gives the end of the last range).
 __host__ __device__ inline long long cta_begin(const GemmGeometry &g, int c) {
     return (g.blocks * c) / g.ctas;

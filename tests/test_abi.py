@@ -173,6 +173,31 @@ SHAPES = [(1, 16, 64, 152), (4, 2048, 7168, 152), (16, 18432, 7168, 152), (16, 1
           (48, 7168, 14336, 152), (33, 130, 72, 152)]
 
 
+@pytest.mark.parametrize("M,N,K,expect_shallow", [
+    (4, 2048, 7168, True), (16, 4096, 7168, True), (32, 4096, 7168, True),
+    (16, 12288, 7168, False), (16, 18432, 7168, False), (16, 7168, 18432, False),
+    (64, 18432, 7168, False), (64, 7168, 14336, False), (3, 200, 136, True)])
+def test_ring_depth_follows_weight_bytes_per_cta(lib, M, N, K, expect_shallow):
+    """With programmatic dependent launch the shallow ring (two CTAs per SM) is
+    taken below 1 MiB of weights per CTA, the deep ring (more bytes in flight)
+    above; without it always the deep ring."""
+    prev = sk.set_pdl(False)
+    try:
+        deep = sk.gemm_plan(M, N, K, 152)
+        sk.set_pdl(True)
+        plan = sk.gemm_plan(M, N, K, 152)
+    finally:
+        sk.set_pdl(prev)
+    per_cta = plan.blocks * 128 * 64 * 2 / plan.ctas
+    assert (per_cta < 2 ** 20) == expect_shallow
+    if expect_shallow:
+        assert plan.stages < deep.stages
+        assert 2 * (plan.smem_bytes + 1024) <= 233472  # two CTAs fit on an SM
+    else:
+        assert (plan.stages, plan.smem_bytes) == (deep.stages, deep.smem_bytes)
+        assert deep.smem_bytes > 233472 // 2
+
+
 @pytest.mark.parametrize("M,N,K,sms", SHAPES)
 def test_work_split_covers_every_block_once(lib, M, N, K, sms):
     plan = sk.gemm_plan(M, N, K, sms)
