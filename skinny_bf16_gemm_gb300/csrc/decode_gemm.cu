@@ -42,10 +42,15 @@ constexpr int kThreads = 192;
 constexpr int kEpilogueThreads = 128;
 constexpr int kWBytes = kBlockN * kBlockK * 2;
 constexpr uint64_t kDrainLimitNs = 200000000ull;  // 0.2 s for copies already issued
-constexpr int kL2PrefetchBlocks = 6;  // weight blocks prefetched to L2 before the ring's
+// Weight blocks prefetched to L2, beyond the ring's first fill, before waiting
+// on the previous kernel: with the shallow ring (short streams) most of the
+// CTA's range, so the stream runs from L2 once the wait is over; with the deep
+// ring a short lead (a longer one slows the previous kernel's last CTAs).
+constexpr int kL2PrefetchShallow = 26, kL2PrefetchDeep = 6;
+constexpr int kMaxShallowStages = 6;  // shallow rings have 4..6 stages, deep ones 9..11
 
 // MP: padded row count (MMA N). STAGES: shared-memory ring depth. The deep ring
-// (~185 KB) keeps the most bytes in flight; the shallow one (~100-112 KB) lets
+// (185-227 KB) keeps the most bytes in flight; the shallow one (~100-112 KB) lets
 // the next kernel's CTAs be resident on the same SM while this one finishes, so
 // with programmatic dependent launch they stream weights across the boundary
 // (plan.cuh use_shallow_ring picks one by the weight bytes per CTA).
@@ -200,7 +205,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tma_load_2d(st, &w_map, bar_full + 8 * j, kb * kBlockK, t * kBlockN, pol_w);
             }
             // The blocks after the ring's worth go to L2 ahead of time.
-            const long long npf = total - npre < kL2PrefetchBlocks ? total - npre : kL2PrefetchBlocks;
+            const long long lead = STAGES <= kMaxShallowStages ? kL2PrefetchShallow : kL2PrefetchDeep;
+            const long long npf = total - npre < lead ? total - npre : lead;
             for (long long j = npre; j < npre + npf; ++j) {
                 const long long blk = b0 + j;
                 ptx::tma_prefetch_l2_2d(&w_map, static_cast<int>(blk % g.kblocks) * kBlockK,
@@ -503,9 +509,14 @@ cudaError_t launch_variant(const CUtensorMap &w_map, const CUtensorMap &x_map,
     return cudaLaunchKernelEx(&cfg, decode_gemm_kernel<MP, STAGES>, w_map, x_map, args);
 }
 
-constexpr int kDeepStages16 = 10, kDeepStages32 = 9, kDeepStages64 = 7;
+// Deep rings: about 185 KB for 16 rows, near the 227 KB a CTA may use for 32 and
+// 64 rows (their x slices take a larger share of each stage). Measured on GB300:
+// 12 stages for 16 rows gain alone but lose inside the layer chain.
+constexpr int kDeepStages16 = 10, kDeepStages32 = 11, kDeepStages64 = 9;
 // Shallow rings sized so two CTAs fit on one SM (about 112, 104 and 100 KB).
 constexpr int kShallowStages16 = 6, kShallowStages32 = 5, kShallowStages64 = 4;
+static_assert(kShallowStages16 <= kMaxShallowStages && kDeepStages64 > kMaxShallowStages,
+              "ring classes must stay apart");
 
 }  // namespace
 
