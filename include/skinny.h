@@ -226,14 +226,17 @@ SKINNY_API int skinny_set_pdl(int enable);
 
 /* ---- host-side planning (no GPU needed) ------------------------------------ */
 
-/* How decode_gemm_bf16 splits a problem over `num_sms` CTAs (stream-K: the
- * ceil(N/128) x ceil(K/64) weight blocks, in tile-major order, are cut into
- * `ctas` contiguous, equal-as-possible ranges). */
+/* How decode_gemm_bf16 splits a problem over `num_sms` CTAs: one whole 128-row
+ * tile per CTA when the tiles fill at least 90 % of the SMs (no split-K), else
+ * stream-K: the ceil(N/128) x ceil(K/64) weight blocks, in tile-major order, are
+ * cut into `ctas` contiguous, equal-as-possible ranges. The ring depth follows
+ * the weight bytes per CTA under the current PDL setting: the shallow ring (two
+ * CTAs per SM) below 1 MiB with PDL on, the deep ring otherwise. */
 typedef struct {
     int tiles;          /* ceil(N / 128): 128-row weight tiles */
     int kblocks;        /* ceil(K / 64): 64-wide K blocks per tile */
     long long blocks;   /* tiles * kblocks */
-    int ctas;           /* CTAs launched: min(num_sms, blocks) */
+    int ctas;           /* CTAs launched: tiles, or min(num_sms, blocks) */
     int mma_n;          /* padded row count the MMA runs with: 16, 32 or 64 */
     int stages;         /* shared-memory pipeline stages per CTA */
     int smem_bytes;     /* dynamic shared memory per CTA */
