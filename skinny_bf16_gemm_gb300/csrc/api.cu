@@ -286,9 +286,16 @@ int gemm_launch_static(const void *x, const void *W, void *out, int M, int N, in
     return SKINNY_OK;
 }
 
-// CTAs per row of the reduce: enough rows x CTAs to spread a small problem over
-// many SMs, fewer (bigger) CTAs once rows alone fill the GPU.
-int reduce_ctas_per_row(int M) { return M <= 32 ? 8 : 4; }
+// CTAs per row of the reduce. An 8-CTA cluster per row spreads a few rows, or
+// heavy ones, over many SMs; with enough light rows one 896-thread CTA per row is
+// faster (no cluster exchange). Loads per thread = TP partial fragments plus the
+// residual's. Chosen from a sweep of 1, 2, 4 and 8 CTAs per row over TP in
+// {2, 4, 8}, M in {1, .., 64}, residual or not, on GB300.
+int reduce_ctas_per_row(int M, int TP, bool residual) {
+    const int loads = TP + (residual ? 1 : 0);
+    if ((M >= 32 && loads <= 8) || (M >= 16 && loads <= 4)) return 1;
+    return 8;
+}
 
 }  // namespace
 }  // namespace skinny
@@ -355,7 +362,7 @@ int reduce_residual_rmsnorm(const void *partials, int TP, const void *residual,
         pdl = g_pdl;
     }
     cudaError_t e = launch_reduce_rmsnorm(partials, TP, residual, gamma, out, residual_out, M, eps,
-                                          reduce_ctas_per_row(M),
+                                          reduce_ctas_per_row(M, TP, residual != nullptr),
                                           static_cast<cudaStream_t>(stream), pdl);
     if (e != cudaSuccess) {
         cudaGetLastError();

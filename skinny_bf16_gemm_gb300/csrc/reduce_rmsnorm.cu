@@ -7,7 +7,8 @@
 // then per row: rstd = rsqrt(sum_c h^2 / 7168 + eps) (FP32) and
 //   out[m][c] = BF16((h * rstd) * gamma[c]).
 //
-// Layout: one cluster of C CTAs per row (grid C x M); CTA r of the cluster owns
+// Layout: one cluster of C CTAs per row (grid C x M; C = 1: one CTA, no cluster,
+// whose 896 threads cover the row); CTA r of the cluster owns
 // the 896 / C 16-byte fragments (8 BF16 each) r*896/C .. ; thread t owns one
 // fragment, so a whole row's TP + 1 loads per thread are in flight at once. The
 // row's sum of squares: an FMA chain over the thread's 8 values, a warp butterfly,
