@@ -53,6 +53,11 @@ def parse():
     ap.add_argument("--sweep-calls", type=int, default=200)
     ap.add_argument("--profile", action="store_true",
                     help="a few launches of each chain kernel, for ncu captures")
+    ap.add_argument("--profile-configs", action="store_true",
+                    help="two launches of every GEMM / reduce / gather config, for a per-call "
+                         "ncu launch list")
+    ap.add_argument("--config-filter", default="",
+                    help="with --profile-configs: only configs whose label contains this")
     return ap.parse_args()
 
 
@@ -363,6 +368,61 @@ def run_sweep(args):
     return 0
 
 
+def run_profile_configs(args):
+    """Every GEMM, reduce and gather config of the sweep, launched twice each
+    (eagerly, one config's buffers at a time), for a per-call ncu launch list
+    with cold caches. Prints the launch order, one label per launch pair."""
+    import __graft_entry__
+    __graft_entry__.build()
+    import skinny_bf16_gemm_gb300 as sk
+    sk.set_pdl(bool(args.pdl))
+    dev = torch.device("cuda", 0)
+    labels = []
+    gemms = ([("gemm pr1", workloads.PR1_GEMM)] + [("gemm sweep", g) for g in workloads.GEMM_SWEEP]
+             + [("gemm lm_head", g) for g in workloads.LM_HEAD]
+             + [("gemm wider", g) for g in workloads.GEMM_WIDER]
+             + [("gemm chain", workloads.CHAIN.gemm1()), ("gemm chain", workloads.CHAIN.gemm2())])
+    for label, g in gemms:
+        name = f"{label} M={g.M} N={g.N} K={g.K}"
+        if args.config_filter not in name:
+            continue
+        inp = workloads.gemm_inputs(g.M, g.N, g.K, workloads.seed_for("cold", g.M, g.N, g.K),
+                                    device=dev)
+        out = torch.empty(g.M, g.N, device=dev, dtype=torch.bfloat16)
+        for _ in range(2):
+            sk.decode_gemm_bf16(inp.x, inp.W, out)
+        torch.cuda.synchronize()
+        labels.append({"label": name, "kernel": "decode_gemm", "bytes": g.algorithmic_bytes()})
+        del inp
+        torch.cuda.empty_cache()
+    reduces = [("reduce pr1", workloads.PR1_REDUCE)] + [("reduce sweep", r) for r in workloads.REDUCE_SWEEP]
+    for label, r in reduces:
+        name = f"{label} TP={r.TP} M={r.M} res={int(r.residual)}"
+        if args.config_filter not in name:
+            continue
+        inp = workloads.reduce_inputs(r.TP, r.M, workloads.seed_for("cold", r.TP, r.M), r.residual,
+                                      device=dev)
+        out = torch.empty(r.M, r.width, device=dev, dtype=torch.bfloat16)
+        rout = torch.empty_like(out)
+        for _ in range(2):
+            sk.reduce_residual_rmsnorm(inp.partials, inp.residual, inp.gamma, out, rout, 1e-6)
+        torch.cuda.synchronize()
+        labels.append({"label": name, "kernel": "reduce_rmsnorm", "bytes": r.algorithmic_bytes()})
+    for TP, M, S in ([(8, m, 896) for m in (1, 16, 64)] + [(8, m, 2560) for m in (1, 8, 32, 64)]):
+        name = f"gather TP={TP} M={M} S={S}"
+        if args.config_filter not in name:
+            continue
+        shards = torch.randn(TP, M, S, device=dev).to(torch.bfloat16)
+        out = torch.empty(M, TP * S, device=dev, dtype=torch.bfloat16)
+        for _ in range(2):
+            sk.gather_shards_bf16(shards, out)
+        torch.cuda.synchronize()
+        labels.append({"label": name, "kernel": "gather", "bytes": 4 * TP * M * S})
+    st, word = sk.device_error(0)
+    print(json.dumps({"profile_configs": labels, "device_error": word}), flush=True)
+    return 0 if st == 0 else 1
+
+
 def run_profile(args):
     """Three launches each of the chain's two decode GEMMs and its reduce, on the
     chain's shapes (weights 264 MB each, larger than L2), for ncu captures."""
@@ -401,6 +461,8 @@ def main():
         return run_sweep(args)
     if args.profile:
         return run_profile(args)
+    if args.profile_configs:
+        return run_profile_configs(args)
 
     import __graft_entry__
     if world > 1:
