@@ -199,8 +199,9 @@ def host_chain_bits(cfg, seed):
             "x0": workloads.bits(inp.x0), "res0": workloads.bits(inp.residual0)}
 
 
-def time_oracle(cfg, budget_s, steps=None, warmup=0, seed=0):
-    """Time the oracle on the chain workload on the host cores.
+def time_oracle(cfg, budget_s, steps=None, warmup=0, seed=0, threads=None):
+    """Time the oracle on the chain workload on the host cores (all of them, or
+    `threads`).
 
     Each step covers sampled GEMM output columns sized to about budget_s of CPU
     work (all columns if a whole step fits). steps=None: repeat steps until about
@@ -209,7 +210,7 @@ def time_oracle(cfg, budget_s, steps=None, warmup=0, seed=0):
     from oracle import build as obuild
     obuild.build()
     bits = host_chain_bits(cfg, seed)
-    threads = oracle.max_threads()
+    threads = oracle.max_threads() if threads is None else threads
     probe = 64
     t0 = time.perf_counter()
     oracle_chain_sample(bits, cfg, np.arange(probe), np.arange(probe), threads)
@@ -684,6 +685,8 @@ def main():
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = {k: v for k, v in time_oracle(cfg, 10.0).items()
                                 if k in ("value", "unit", "cores", "kind", "sample")}
+        one = time_oracle(cfg, 5.0, threads=1)
+        line["cpu_baseline"]["one_thread"] = {"value": one["value"], "sample": one["sample"]}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
