@@ -199,6 +199,43 @@ def host_chain_bits(cfg, seed):
             "x0": workloads.bits(inp.x0), "res0": workloads.bits(inp.residual0)}
 
 
+def chain_parity(inp, cfg, sk, samples=512, seed=0):
+    """The oracle beside the GPU on the timed chain's own inputs (part of the CPU
+    baseline leg): layer 0's two GEMMs on sampled output columns, with the ulp
+    histogram of the GEMM tolerance, and layer 0's reduce + residual + RMSNorm on
+    whole rows (residual bit for bit, out in ulps)."""
+    import oracle
+    from oracle import compare
+    dev = inp.x0.device
+    rng = np.random.default_rng(seed)
+    h1 = torch.empty(cfg.M, cfg.ffn, dtype=torch.bfloat16, device=dev)
+    parts = torch.empty(cfg.TP, cfg.M, cfg.hidden, dtype=torch.bfloat16, device=dev)
+    parts[1:].copy_(inp.peers[0])
+    out = torch.empty(cfg.M, cfg.hidden, dtype=torch.bfloat16, device=dev)
+    rout = torch.empty_like(out)
+    sk.decode_gemm_bf16(inp.x0, inp.W1[0], h1)
+    sk.decode_gemm_bf16(h1, inp.W2[0], parts[0])
+    sk.reduce_residual_rmsnorm(parts, inp.residual0, inp.gamma[0], out, rout, cfg.eps)
+    torch.cuda.synchronize()
+    report = {}
+    for name, x, W, y in (("gemm1", inp.x0, inp.W1[0], h1), ("gemm2", h1, inp.W2[0], parts[0])):
+        cols = np.sort(rng.choice(W.shape[0], size=min(samples, W.shape[0]), replace=False))
+        wsel = workloads.bits(W[torch.as_tensor(cols, device=dev, dtype=torch.long)])
+        xb = workloads.bits(x)
+        idx = np.arange(cols.size, dtype=np.int32)
+        ref = oracle.decode_gemm(xb, wsel, cols=idx)
+        ssum, asum = oracle.decode_gemm_f64(xb, wsel, cols=idx)
+        rep_ = compare.gemm_check(workloads.bits(y)[:, cols], ref, ssum, asum)
+        report[name] = {k: rep_[k] for k in ("ok", "n", "within1_frac", "max_judged",
+                                             "literal_hist", "literal_max")}
+    want_h = oracle.reduce_residual(workloads.bits(parts), workloads.bits(inp.residual0))
+    want_o = oracle.rmsnorm(want_h, workloads.bits(inp.gamma[0]), cfg.eps)
+    d = compare.ulp_distance(workloads.bits(out), want_o)
+    report["reduce"] = {"residual_bit_exact": compare.bits_equal(workloads.bits(rout), want_h),
+                        "out_ulp_hist": compare.histogram(d), "out_ulp_max": int(d.max())}
+    return report
+
+
 def time_oracle(cfg, budget_s, steps=None, warmup=0, seed=0, threads=None):
     """Time the oracle on the chain workload on the host cores (all of them, or
     `threads`).
@@ -687,6 +724,7 @@ def main():
                                 if k in ("value", "unit", "cores", "kind", "sample")}
         one = time_oracle(cfg, 5.0, threads=1)
         line["cpu_baseline"]["one_thread"] = {"value": one["value"], "sample": one["sample"]}
+        line["parity"] = chain_parity(inp, cfg, sk)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
