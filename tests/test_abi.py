@@ -170,7 +170,8 @@ SHAPES = [(1, 16, 64, 152), (4, 2048, 7168, 152), (16, 18432, 7168, 152), (16, 1
           (16, 7168, 18432, 152), (32, 20480, 7168, 152), (3, 200, 136, 152),
           (8, 128, 64, 152), (5, 12288, 7168, 148), (2, 4096, 7168, 7), (1, 1, 8, 152),
           (32, 1000, 1000, 152), (7, 300, 4096, 64), (64, 18432, 7168, 152),
-          (48, 7168, 14336, 152), (33, 130, 72, 152)]
+          (48, 7168, 14336, 152), (33, 130, 72, 152), (8, 65536, 2048, 152),
+          (3, 40000, 1000, 152)]
 
 
 @pytest.mark.parametrize("M,N,K,expect_shallow", [

@@ -79,6 +79,15 @@ def test_gemm_full_size_sampled(cuda_ok, M, N, K):
     check_gemm_sampled(x, W, out, sample_columns(N, seed=M * 7 + N))
 
 
+@pytest.mark.parametrize("M,N,K", [(8, 65536, 2048), (3, 40000, 1000)])
+def test_gemm_many_tiles_per_cta(cuda_ok, M, N, K):
+    """More 128-row tiles than SMs several times over (a vocabulary-sized N):
+    every CTA's range holds whole tiles between split ends; ragged N and K."""
+    x, W = gemm_inputs_device(M, N, K, workloads.seed_for("many", M, N, K))
+    out = run_gemm(x, W)
+    check_gemm_sampled(x, W, out, sample_columns(N, count=768, seed=N))
+
+
 def test_gemm_deterministic(cuda_ok):
     x, W = gemm_inputs_device(8, 4096, 7168, 11)
     a = run_gemm(x, W)
