@@ -1,14 +1,14 @@
 // Decode GEMM for GB300 (sm_103a): out[M, N] = x[M, K] @ W[N, K]^T, BF16 operands,
 // FP32 accumulation, one BF16 rounding ("drafter/linears": module text and
-// DraftGemm). M <= 32, so the time is the weight stream: every byte of W is read
+// DraftGemm). M <= 64, so the time is the weight stream: every byte of W is read
 // once from HBM by TMA and fed to the tensor cores while it is on chip.
 //
-// One persistent CTA per SM, 192 threads in three roles:
+// Persistent CTAs of 192 threads in three roles:
 //   warp 0      TMA producer: W tiles [128 rows x 64 K] and x slices [MP x 64 K]
 //               into a ring of STAGES shared-memory stages (128-byte swizzle);
 //   warp 1      MMA issuer: tcgen05.mma kind::f16, M = 128 weight rows, N = MP
-//               (x rows padded to 16 or 32; the padding rows are TMA zero fill),
-//               accumulating in tensor memory (two 32-column buffers);
+//               (x rows padded to 16, 32 or 64; the padding rows are TMA zero
+//               fill), accumulating in tensor memory (two accumulator buffers);
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator (TMEM lane = weight row =
 //               output column n, column = output row m), one BF16 rounding, or
 //               the split-K fix-up.
@@ -19,9 +19,12 @@
 // is the last piece): the others publish their FP32 partials behind a release
 // flag, and the finisher adds them in K order, so the bits do not depend on
 // timing.
-// Before waiting on the previous kernel in the stream (programmatic dependent
-// launch) the producer already streams the first STAGES weight tiles: weights
-// never depend on the previous kernel, x may.
+// Ring depth (plan.cuh use_shallow_ring): the deep ring, one CTA per SM, for
+// long streams; the shallow ring for short ones under programmatic dependent
+// launch, so that the next kernel's CTA shares the SM. Before waiting on the
+// previous kernel in the stream the producer already streams the first STAGES
+// weight tiles and prefetches more into L2: weights never depend on the previous
+// kernel, x may.
 // Every wait is bounded (wait_limit_ns); a role that gives up records a bit in
 // the device error word, the CTA drains its in-flight copies and MMAs, frees its
 // tensor memory and exits.
