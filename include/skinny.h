@@ -219,8 +219,11 @@ SKINNY_API int skinny_device_error(int device, int *word);
  *   decode_gemm_bf16, gamma of reduce_residual_rmsnorm -- before waiting for its
  *   predecessor, and everything else after ("drafter/comm", ArNorm.kernel: gamma
  *   is loaded before the launch_dependents / wait pair, the rows after it). So
- *   with PDL on, W and gamma must not be written by the kernel just before the
- *   call on the same stream. Off by default. Returns the previous setting.
+ *   with PDL on, W and gamma must not be written by any kernel that may still be
+ *   running on the stream when the call is made (every kernel of this library
+ *   lets its successor start early, so more than one predecessor can still be in
+ *   flight): write weights before the chain of calls. Off by default. Returns
+ *   the previous setting.
  */
 SKINNY_API int skinny_set_pdl(int enable);
 
