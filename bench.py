@@ -47,6 +47,9 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--pdl", type=int, default=1, help="programmatic dependent launch")
     ap.add_argument("--graph", type=int, default=0, help="replay the step as a CUDA graph")
+    ap.add_argument("--fused", type=int, default=1,
+                    help="each layer's second GEMM and reduce + RMSNorm through "
+                         "decode_gemm_bf16_reduce_rmsnorm (bit-identical; 0: the two calls)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true",
                     help="per-config GB/s of every GEMM and reduce config instead of the chain")
@@ -519,7 +522,8 @@ def main():
     device = torch.device("cuda", local)
     from skinny_bf16_gemm_gb300.replicas import replica_seed
     inp = workloads.chain_inputs(cfg, replica_seed(workloads.seed_for("chain"), rank), device=device)
-    chain = LayerChain(inp.W1, inp.W2, inp.peers, inp.gamma, cfg.M, cfg.eps, device=device)
+    chain = LayerChain(inp.W1, inp.W2, inp.peers, inp.gamma, cfg.M, cfg.eps, device=device,
+                       fused=bool(args.fused))
     chain.x.copy_(inp.x0)
     chain.res_in.copy_(inp.residual0)
     sk.set_pdl(bool(args.pdl))
@@ -644,7 +648,8 @@ def main():
     h2d = (host_x.numel() + host_res.numel() + sum(p.numel() for p in host_peers)) * 2
     d2h = (host_out[0].numel() + host_res_out[0].numel()) * 2
     e2e_steps = max(1, min(args.steps, 500))
-    chains = [chain, LayerChain(inp.W1, inp.W2, inp.peers, inp.gamma, cfg.M, cfg.eps, device=device)]
+    chains = [chain, LayerChain(inp.W1, inp.W2, inp.peers, inp.gamma, cfg.M, cfg.eps, device=device,
+                                fused=bool(args.fused))]
     copy_stream = torch.cuda.Stream()
     inputs_ready = [torch.cuda.Event() for _ in range(2)]
     done = [torch.cuda.Event() for _ in range(2)]
@@ -699,6 +704,7 @@ def main():
         "data": "synthetic (seeded N(0,1) activations, N(0,1/K) weights)",
         "impl": "ours",
         "config": workload_config(cfg, {"pdl": bool(args.pdl), "graph": bool(args.graph),
+                                        "fused_gemm_reduce": bool(args.fused),
                                         "parallelism": "replicas" if world > 1 else "single"}),
         "hbm_frac_of_measured": value / peak,
         "hbm_frac_of_nominal_8000": value / 8000.0,
@@ -709,8 +715,8 @@ def main():
                      if peak_kind == "measured" else "fallback 6800 GB/s",
                      "algorithmic_bytes_per_launch": gemm_bytes,
                      "avg_launch_ms": gemm_ms, "launches_timed": gemm_launches,
-                     "timing": "back-to-back launches of the chain's 6 GEMMs, CUDA events "
-                               "around the loop, PDL as in the timed region"},
+                     "timing": "back-to-back launches of the chain's 6 GEMMs (decode_gemm_bf16), "
+                               "CUDA events around the loop, PDL as in the timed region"},
         "kernels": {"decode_gemm_avg_us": gemm_ms * 1e3, "reduce_rmsnorm_avg_us": reduce_ms * 1e3,
                     "reduce_algorithmic_bytes": cfg.reduce().algorithmic_bytes(),
                     "reduce_gbs": cfg.reduce().algorithmic_bytes() / (reduce_ms * 1e-3) / 1e9},

@@ -174,6 +174,39 @@ SKINNY_API int reduce_residual_rmsnorm(const void *partials, int TP, const void 
                             const void *gamma, void *out, void *residual_out,
                             int M, float eps, void *stream);
 
+/*
+ * decode_gemm_bf16_reduce_rmsnorm -- a row-parallel drafter linear whose output
+ *   rows are this rank's partial of the TP all-reduce, with that all-reduce's
+ *   local stand-in and the RMSNorm that follows ("drafter/comm" module text: each
+ *   layer's row-parallel linear ends in the TP all-reduce fused with the next
+ *   RMSNorm; ArNorm for the arithmetic; "drafter/linears" DraftGemm for the
+ *   GEMM). Computes what decode_gemm_bf16(x, W, partials[0], M, 7168, K)
+ *   followed by reduce_residual_rmsnorm(partials, TP, residual, gamma, out,
+ *   residual_out, M, eps) compute, bit for bit, with two kernels instead of
+ *   three phases: the GEMM leaves every split-K partial in the library's scratch
+ *   without finishing any tile, and the reduce kernel adds each column's
+ *   partials in K order (the GEMM's own order), rounds once into slot 0 and goes
+ *   on with the rank-order sum, residual and RMSNorm.
+ *
+ *   x             [M, K] BF16 row-major; W [7168, K] BF16 row-major.
+ *   partials      [TP, M, 7168] BF16, contiguous. Slot 0 is written with the
+ *                 GEMM's rows; slots 1..TP-1 (the other ranks' rows) are read.
+ *   residual      [M, 7168] BF16 or NULL; gamma [7168] BF16.
+ *   out           [M, 7168] BF16: RMSNorm(residual_out) * gamma.
+ *   residual_out  [M, 7168] BF16: the new residual; may be the same pointer as
+ *                 residual (in place), no other overlap between any output and
+ *                 any input or between outputs.
+ *   All pointers 16-byte aligned. 1 <= M <= 64; 1 <= TP <= 8; K >= 8 and
+ *   K % 8 == 0; eps > 0, finite. Needs at least 56 SMs. Uses the decode GEMM's
+ *   per-device scratch, like decode_gemm_bf16 (same rules on streams).
+ *   Errors: SKINNY_ERR_NULL, _SHAPE, _ALIGN, _ALIAS, _ARG, _DEVICE, _CAPTURE,
+ *   _ALLOC, _LAUNCH.
+ */
+SKINNY_API int decode_gemm_bf16_reduce_rmsnorm(const void *x, const void *W, void *partials,
+                                               int TP, const void *residual, const void *gamma,
+                                               void *out, void *residual_out, int M, int K,
+                                               float eps, void *stream);
+
 /* Largest TP and row count of gather_shards_bf16. */
 #define SKINNY_GATHER_MAX_TP 64
 #define SKINNY_GATHER_MAX_M 65535

@@ -60,6 +60,9 @@ def load_library(path: str = LIBRARY):
     lib.reduce_residual_rmsnorm.restype = i32
     lib.decode_gemm_bf16_logits.argtypes = [vp, vp, vp, i32, i32, i32, i32, f32, f32, vp]
     lib.decode_gemm_bf16_logits.restype = i32
+    lib.decode_gemm_bf16_reduce_rmsnorm.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, i32, i32,
+                                                    f32, vp]
+    lib.decode_gemm_bf16_reduce_rmsnorm.restype = i32
     lib.gather_shards_bf16.argtypes = [vp, i32, i32, i32, vp, vp]
     lib.gather_shards_bf16.restype = i32
     lib.skinny_status_string.argtypes = [i32]
@@ -164,6 +167,38 @@ def reduce_residual_rmsnorm(partials, residual, gamma, out, residual_out, eps=1e
         gamma.data_ptr(), out.data_ptr(), residual_out.data_ptr(), M, float(eps),
         _stream_handle(stream))
     _check(st, "reduce_residual_rmsnorm")
+    return out, residual_out
+
+
+def decode_gemm_bf16_reduce_rmsnorm(x, W, partials, residual, gamma, out, residual_out,
+                                    eps=1e-6, stream=None):
+    """The row-parallel linear with the reduce + residual + RMSNorm after it.
+
+    x [M, K], W [7168, K]; partials [TP, M, 7168] (slot 0 receives x @ W^T,
+    slots 1.. are read); residual [M, 7168] or None; gamma [7168]; out and
+    residual_out [M, 7168]; all contiguous CUDA bfloat16. Returns
+    (out, residual_out), bit for bit those of decode_gemm_bf16 followed by
+    reduce_residual_rmsnorm.
+    """
+    _bf16_cuda(x, "x")
+    _bf16_cuda(W, "W")
+    _bf16_cuda(partials, "partials")
+    if x.dim() != 2 or W.dim() != 2 or tuple(W.shape) != (HIDDEN, x.shape[1]):
+        raise ValueError(f"x must be [M, K] and W [{HIDDEN}, K]")
+    M, K = x.shape
+    if partials.dim() != 3 or tuple(partials.shape[1:]) != (M, HIDDEN):
+        raise ValueError(f"partials must be [TP, {M}, {HIDDEN}], got {tuple(partials.shape)}")
+    TP = partials.shape[0]
+    if residual is not None:
+        _bf16_cuda(residual, "residual", (M, HIDDEN))
+    _bf16_cuda(gamma, "gamma", (HIDDEN,))
+    _bf16_cuda(out, "out", (M, HIDDEN))
+    _bf16_cuda(residual_out, "residual_out", (M, HIDDEN))
+    st = load_library().decode_gemm_bf16_reduce_rmsnorm(
+        x.data_ptr(), W.data_ptr(), partials.data_ptr(), TP,
+        None if residual is None else residual.data_ptr(), gamma.data_ptr(), out.data_ptr(),
+        residual_out.data_ptr(), M, K, float(eps), _stream_handle(stream))
+    _check(st, "decode_gemm_bf16_reduce_rmsnorm")
     return out, residual_out
 
 

@@ -9,18 +9,23 @@ partial rows are local slots, the one-GPU stand-in of "cutedsl/common/twoshot"):
     out, residual   = reduce_residual_rmsnorm(partials[l], residual, gamma[l])
     x               = out
 
-Slots 1..TP-1 of partials[l] hold the other ranks' rows. Every step of the chain
-runs in the library's kernels; this class only owns the device buffers and
-orders the calls on one stream (optionally as one CUDA graph).
+Slots 1..TP-1 of partials[l] hold the other ranks' rows. With fused=True the
+second GEMM and the reduce + residual + RMSNorm are one call,
+decode_gemm_bf16_reduce_rmsnorm (bit-identical results, two kernels instead of a
+split-K fix-up inside the GEMM plus a reduce). Every step of the chain runs in
+the library's kernels; this class only owns the device buffers and orders the
+calls on one stream (optionally as one CUDA graph).
 """
 import torch
 
-from . import decode_gemm_bf16, reduce_residual_rmsnorm, set_pdl
+from . import (decode_gemm_bf16, decode_gemm_bf16_reduce_rmsnorm, reduce_residual_rmsnorm,
+               set_pdl)
 
 
 class LayerChain:
-    def __init__(self, W1, W2, peers, gamma, M, eps=1e-6, device="cuda"):
+    def __init__(self, W1, W2, peers, gamma, M, eps=1e-6, device="cuda", fused=False):
         self.layers = len(W1)
+        self.fused = fused
         self.W1, self.W2, self.gamma = W1, W2, gamma
         self.M, self.eps = M, eps
         self.F, self.H = W1[0].shape
@@ -56,15 +61,21 @@ class LayerChain:
             if on_launch:
                 on_launch("gemm", l, "after")
                 on_launch("gemm", l, "before")
-            decode_gemm_bf16(self.h1, self.W2[l], self.partials[l][0], stream)
-            if on_launch:
-                on_launch("gemm", l, "after")
-                on_launch("reduce", l, "before")
             out, res_out = self.outs[l % 2], self.res[l % 2]
-            reduce_residual_rmsnorm(self.partials[l], res, self.gamma[l], out, res_out,
-                                    self.eps, stream)
-            if on_launch:
-                on_launch("reduce", l, "after")
+            if self.fused:
+                decode_gemm_bf16_reduce_rmsnorm(self.h1, self.W2[l], self.partials[l], res,
+                                                self.gamma[l], out, res_out, self.eps, stream)
+                if on_launch:
+                    on_launch("gemm", l, "after")
+            else:
+                decode_gemm_bf16(self.h1, self.W2[l], self.partials[l][0], stream)
+                if on_launch:
+                    on_launch("gemm", l, "after")
+                    on_launch("reduce", l, "before")
+                reduce_residual_rmsnorm(self.partials[l], res, self.gamma[l], out, res_out,
+                                        self.eps, stream)
+                if on_launch:
+                    on_launch("reduce", l, "after")
             x, res = out, res_out
         return x, res
 

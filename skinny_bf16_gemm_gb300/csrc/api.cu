@@ -190,7 +190,7 @@ int gemm_launch(const void *x, const void *W, void *out, int M, int N, int K, vo
     if ((st = encode_2d(enc, &w_map, W, N, K, kBlockN))) return st;
     if ((st = encode_2d(enc, &x_map, x, M, K, mma_n))) return st;
     const GemmGeometry g = make_geometry(M, N, K, choose_ctas(N, d->sms));
-    GemmArgs a;
+    GemmArgs a = {};
     a.M = M;
     a.N = N;
     a.K = K;
@@ -258,7 +258,7 @@ int gemm_launch_static(const void *x, const void *W, void *out, int M, int N, in
         cudaGetLastError();
         return SKINNY_ERR_LAUNCH;
     }
-    GemmArgs a;
+    GemmArgs a = {};
     a.M = M;
     a.N = N;
     a.K = K;
@@ -311,6 +311,91 @@ int decode_gemm_bf16(const void *x, const void *W, void *out, int M, int N, int 
 int decode_gemm_bf16_noalloc(const void *x, const void *W, void *out, int M, int N, int K,
                              void *stream) {
     return gemm_launch_static(x, W, out, M, N, K, stream);
+}
+
+int decode_gemm_bf16_reduce_rmsnorm(const void *x, const void *W, void *partials, int TP,
+                                    const void *residual, const void *gamma, void *out,
+                                    void *residual_out, int M, int K, float eps, void *stream) {
+    constexpr int N = SKINNY_HIDDEN;
+    if (!x || !W || !partials || !gamma || !out || !residual_out) return SKINNY_ERR_NULL;
+    if (M < 1 || M > SKINNY_REDUCE_MAX_M || TP < 1 || TP > SKINNY_REDUCE_MAX_TP) return SKINNY_ERR_SHAPE;
+    int st = gemm_shape_ok(M, N, K);
+    if (st) return st;
+    if (!(eps > 0.0f) || !std::isfinite(eps)) return SKINNY_ERR_ARG;
+    if (!aligned(x, 16) || !aligned(W, 16) || !aligned(partials, 16) || !aligned(gamma, 16) ||
+        !aligned(out, 16) || !aligned(residual_out, 16) || (residual && !aligned(residual, 16)))
+        return SKINNY_ERR_ALIGN;
+    const size_t xb = static_cast<size_t>(M) * K * 2, wb = static_cast<size_t>(N) * K * 2;
+    const size_t row = static_cast<size_t>(M) * N * 2, pb = row * TP, gb = N * 2;
+    // Slot 0 of partials, out and residual_out are written; residual_out may be
+    // residual itself (element-wise in place), nothing else may overlap.
+    if (overlaps(partials, pb, x, xb) || overlaps(partials, pb, W, wb) ||
+        overlaps(partials, pb, gamma, gb) || overlaps(out, row, x, xb) ||
+        overlaps(out, row, W, wb) || overlaps(out, row, partials, pb) ||
+        overlaps(out, row, gamma, gb) || overlaps(out, row, residual_out, row) ||
+        overlaps(residual_out, row, x, xb) || overlaps(residual_out, row, W, wb) ||
+        overlaps(residual_out, row, partials, pb) || overlaps(residual_out, row, gamma, gb) ||
+        (residual && (overlaps(out, row, residual, row) || overlaps(partials, pb, residual, row) ||
+                      (residual != residual_out && overlaps(residual_out, row, residual, row)))))
+        return SKINNY_ERR_ALIAS;
+    int dev;
+    if ((st = current_device(&dev))) return st;
+    if ((st = check_device_pointer(x, dev)) || (st = check_device_pointer(W, dev)) ||
+        (st = check_device_pointer(partials, dev)) || (st = check_device_pointer(gamma, dev)) ||
+        (st = check_device_pointer(out, dev)) || (st = check_device_pointer(residual_out, dev)) ||
+        (residual && (st = check_device_pointer(residual, dev))))
+        return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    DeviceState *d = nullptr;
+    if ((st = ensure_scratch(dev, s, &d))) return st;
+    const GemmGeometry g = make_geometry(M, N, K, choose_ctas(N, d->sms));
+    // The scratch holds two partial slots per CTA: every CTA's range must touch
+    // at most two tiles, which at least one CTA per tile guarantees.
+    if (g.ctas < g.tiles) return SKINNY_ERR_DEVICE;
+    EncodeTiledFn enc;
+    if ((st = encoder(&enc))) return st;
+    const int mma_n = mma_n_for(M);
+    alignas(64) CUtensorMap w_map, x_map;
+    if ((st = encode_2d(enc, &w_map, W, N, K, kBlockN))) return st;
+    if ((st = encode_2d(enc, &x_map, x, M, K, mma_n))) return st;
+    bool pdl;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        pdl = g_pdl;
+    }
+    GemmArgs a = {};
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.out = static_cast<uint16_t *>(partials);
+    a.partials = d->partials;
+    a.slot_floats = kSlotFloats;
+    a.flags = d->flags;
+    a.err = d->err;
+    a.wait_limit_ns = kWaitLimitNs;
+    a.scale = 1.0f;
+    a.publish_only = 1;
+    if (launch_decode_gemm(w_map, x_map, a, mma_n, g.ctas, s, pdl, use_shallow_ring(g, pdl), dev) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return SKINNY_ERR_LAUNCH;
+    }
+    SplitKPartials fix;
+    fix.partials = d->partials;
+    fix.slot_floats = kSlotFloats;
+    fix.M = M;
+    fix.N = N;
+    fix.K = K;
+    fix.ctas = g.ctas;
+    // The same CTAs per row as reduce_residual_rmsnorm: the same order of the sum
+    // of squares, so out is bit-identical to the two separate calls.
+    const int cpr = reduce_ctas_per_row(M, TP, residual != nullptr);
+    if (launch_reduce_rmsnorm_splitk(partials, TP, residual, gamma, out, residual_out, M, eps, cpr,
+                                     fix, s, pdl) != cudaSuccess) {
+        cudaGetLastError();
+        return SKINNY_ERR_LAUNCH;
+    }
+    return SKINNY_OK;
 }
 
 int decode_gemm_bf16_logits(const void *x, const void *W, void *out, int M, int N, int K,

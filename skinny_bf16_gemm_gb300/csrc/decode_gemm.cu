@@ -404,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_arrive(bar_acc_empty + 8 * b);  // the MMA may reuse this buffer
 
             const int n = p.tile * kBlockN + row;
-            if (p.kb0 == 0 && p.kb1 == g.kblocks) {
+            if (p.kb0 == 0 && p.kb1 == g.kblocks && !args.publish_only) {
                 // Whole tile in this CTA: round once and store.
                 if (n < g.N) {
 #pragma unroll
@@ -417,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             int first, last;
             tile_contributors(g, p.tile, first, last);
-            if (first == cta) {
+            if (first == cta && !args.publish_only) {
                 // The tile starts in this CTA's range: this CTA finishes it.
                 if (!finish_tile(p.tile, first, last, acc)) break;
                 continue;
@@ -429,6 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int m = 0; m < MP; ++m)
                 if (m < g.M) __stcg(mine + m * kBlockN + row, acc[m]);
+            if (args.publish_only) continue;  // read by the next kernel, after this grid
             ptx::fence_proxy_async_global();
             ptx::named_barrier_sync(1, kEpilogueThreads);
             // One release (fence + store) after the barrier covers every thread's

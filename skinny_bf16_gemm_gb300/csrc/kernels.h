@@ -30,6 +30,18 @@ struct GemmArgs {
     // : v; v *= scale; applied to the FP32 sum before the one BF16 rounding.
     int logits;
     float soft_cap, scale;
+    // 1: every piece, whole tiles included, leaves its FP32 partial in its scratch
+    // slot and nothing is finished here (no flags): the reduce kernel that follows
+    // adds them (decode_gemm_bf16_reduce_rmsnorm).
+    int publish_only;
+};
+
+// Where the reduce kernel finds a publish-only GEMM's partials of the 7168
+// slot-0 columns: the GEMM's geometry (tiles, K blocks, CTAs) and scratch.
+struct SplitKPartials {
+    const float *partials;  // [2 * ctas][slot_floats]
+    int slot_floats;
+    int M, N, K, ctas;
 };
 
 // Pipeline depth and shared memory of the decode GEMM for a padded row count,
@@ -64,6 +76,13 @@ cudaError_t static_scratch_for_current_device(StaticScratch *out);
 cudaError_t launch_reduce_rmsnorm(const void *partials, int TP, const void *residual,
                                   const void *gamma, void *out, void *residual_out, int M,
                                   float eps, int ctas_per_row, cudaStream_t stream, bool pdl);
+
+// The same with slot 0 made from a publish-only GEMM's FP32 partials (added in
+// K order, rounded once, and written to slot 0 of `partials`).
+cudaError_t launch_reduce_rmsnorm_splitk(void *partials, int TP, const void *residual,
+                                         const void *gamma, void *out, void *residual_out, int M,
+                                         float eps, int ctas_per_row, const SplitKPartials &fix,
+                                         cudaStream_t stream, bool pdl);
 
 // Gather TP shards [TP, M, S] into rows [M, TP * S] (S a multiple of 8).
 cudaError_t launch_gather(const void *shards, int TP, int M, int S, void *out,

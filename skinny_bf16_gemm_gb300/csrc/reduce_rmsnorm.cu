@@ -20,6 +20,7 @@
 #include <cuda_runtime.h>
 
 #include "kernels.h"
+#include "plan.cuh"
 #include "ptx.cuh"
 
 namespace skinny {
@@ -56,11 +57,16 @@ __device__ __forceinline__ uint4 pack8(const uint32_t (&b)[8]) {
                       b[6] | (b[7] << 16));
 }
 
-template <int C, bool RES>
+// FIX: slot 0 is not read but made here from a publish-only decode GEMM's FP32
+// partials ("drafter/linears": FP32 split-K partials, one BF16 rounding): the
+// partials of the fragment's 8 columns added in K order and rounded once, as the
+// GEMM's own finisher would; the result is also stored to slot 0.
+template <int C, bool RES, bool FIX>
 __global__ void __launch_bounds__(ReduceShape<C>::kThreads)
-    reduce_rmsnorm_kernel(const uint4 *__restrict__ partials, int TP, const uint4 *residual,
+    reduce_rmsnorm_kernel(const uint4 *partials, int TP, const uint4 *residual,
                           const uint4 *__restrict__ gamma, uint4 *__restrict__ out,
-                          uint4 *residual_out, int M, float eps) {
+                          uint4 *residual_out, int M, float eps, uint4 *slot0,
+                          SplitKPartials fix) {
     using R = ReduceShape<C>;
     __shared__ float warp_sums[R::kWarps];
     __shared__ float parts[C];
@@ -90,12 +96,53 @@ __global__ void __launch_bounds__(ReduceShape<C>::kThreads)
         uint4 pv[kMaxTP];
 #pragma unroll
         for (int r = 0; r < kMaxTP; ++r)
-            if (r < TP) pv[r] = __ldcs(partials + static_cast<size_t>(r) * M * kRowFrags + row_off);
+            if (r < TP && (!FIX || r > 0))
+                pv[r] = __ldcs(partials + static_cast<size_t>(r) * M * kRowFrags + row_off);
         uint4 rv = make_uint4(0, 0, 0, 0);
         if constexpr (RES) rv = __ldcs(residual + row_off);
 
         float s[8];
-        unpack8(pv[0], s);  // the sum starts from slot 0 (keeps -0)
+        if constexpr (FIX) {
+            const GemmGeometry g = make_geometry(fix.M, fix.N, fix.K, fix.ctas);
+            const int col = frag * 8;
+            const int t = col / kBlockN;
+            int first, last;
+            tile_contributors(g, t, first, last);
+            // Partials of up to kU contributors in flight together (fewer with
+            // 896-thread CTAs, whose register budget is smaller).
+            constexpr int kU = C == 1 ? 2 : 4;
+            float a[8];
+            for (int c0 = first; c0 <= last; c0 += kU) {
+                float4 v[kU][2];
+#pragma unroll
+                for (int q = 0; q < kU; ++q) {
+                    if (c0 + q <= last) {
+                        const float4 *src = reinterpret_cast<const float4 *>(
+                            fix.partials + static_cast<size_t>(partial_slot(g, c0 + q, t)) * fix.slot_floats +
+                            row * kBlockN + (col % kBlockN));
+                        v[q][0] = __ldcg(src);
+                        v[q][1] = __ldcg(src + 1);
+                    }
+                }
+#pragma unroll
+                for (int q = 0; q < kU; ++q) {
+                    if (c0 + q > last) break;
+                    const float u[8] = {v[q][0].x, v[q][0].y, v[q][0].z, v[q][0].w,
+                                        v[q][1].x, v[q][1].y, v[q][1].z, v[q][1].w};
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) a[j] = c0 + q == first ? u[j] : __fadd_rn(a[j], u[j]);
+                }
+            }
+            uint32_t s0[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                s0[j] = bf16_bits(a[j]);
+                s[j] = __uint_as_float(s0[j] << 16);
+            }
+            slot0[row_off] = pack8(s0);
+        } else {
+            unpack8(pv[0], s);  // the sum starts from slot 0 (keeps -0)
+        }
 #pragma unroll
         for (int r = 1; r < kMaxTP; ++r) {
             if (r < TP) {
@@ -163,10 +210,10 @@ __global__ void __launch_bounds__(ReduceShape<C>::kThreads)
     }
 }
 
-template <int C, bool RES>
+template <int C, bool RES, bool FIX>
 cudaError_t launch_c(const void *partials, int TP, const void *residual, const void *gamma,
                      void *out, void *residual_out, int M, float eps, cudaStream_t stream,
-                     bool pdl) {
+                     bool pdl, const SplitKPartials &fix) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(C, M, 1);
     cfg.blockDim = dim3(ReduceShape<C>::kThreads, 1, 1);
@@ -188,22 +235,36 @@ cudaError_t launch_c(const void *partials, int TP, const void *residual, const v
     }
     cfg.attrs = attr;
     cfg.numAttrs = n;
-    return cudaLaunchKernelEx(&cfg, reduce_rmsnorm_kernel<C, RES>,
+    return cudaLaunchKernelEx(&cfg, reduce_rmsnorm_kernel<C, RES, FIX>,
                               static_cast<const uint4 *>(partials), TP,
                               static_cast<const uint4 *>(residual),
                               static_cast<const uint4 *>(gamma), static_cast<uint4 *>(out),
-                              static_cast<uint4 *>(residual_out), M, eps);
+                              static_cast<uint4 *>(residual_out), M, eps,
+                              const_cast<uint4 *>(static_cast<const uint4 *>(partials)), fix);
 }
 
-template <int C>
+template <int C, bool FIX>
 cudaError_t launch_res(const void *partials, int TP, const void *residual, const void *gamma,
                        void *out, void *residual_out, int M, float eps, cudaStream_t stream,
-                       bool pdl) {
+                       bool pdl, const SplitKPartials &fix) {
     if (residual)
-        return launch_c<C, true>(partials, TP, residual, gamma, out, residual_out, M, eps,
-                                 stream, pdl);
-    return launch_c<C, false>(partials, TP, residual, gamma, out, residual_out, M, eps, stream,
-                              pdl);
+        return launch_c<C, true, FIX>(partials, TP, residual, gamma, out, residual_out, M, eps,
+                                      stream, pdl, fix);
+    return launch_c<C, false, FIX>(partials, TP, residual, gamma, out, residual_out, M, eps,
+                                   stream, pdl, fix);
+}
+
+template <bool FIX>
+cudaError_t launch_any(const void *partials, int TP, const void *residual, const void *gamma,
+                       void *out, void *residual_out, int M, float eps, int ctas_per_row,
+                       cudaStream_t stream, bool pdl, const SplitKPartials &fix) {
+    switch (ctas_per_row) {
+        case 1: return launch_res<1, FIX>(partials, TP, residual, gamma, out, residual_out, M, eps, stream, pdl, fix);
+        case 2: return launch_res<2, FIX>(partials, TP, residual, gamma, out, residual_out, M, eps, stream, pdl, fix);
+        case 4: return launch_res<4, FIX>(partials, TP, residual, gamma, out, residual_out, M, eps, stream, pdl, fix);
+        case 8: return launch_res<8, FIX>(partials, TP, residual, gamma, out, residual_out, M, eps, stream, pdl, fix);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace
@@ -211,13 +272,17 @@ cudaError_t launch_res(const void *partials, int TP, const void *residual, const
 cudaError_t launch_reduce_rmsnorm(const void *partials, int TP, const void *residual,
                                   const void *gamma, void *out, void *residual_out, int M,
                                   float eps, int ctas_per_row, cudaStream_t stream, bool pdl) {
-    switch (ctas_per_row) {
-        case 1: return launch_res<1>(partials, TP, residual, gamma, out, residual_out, M, eps, stream, pdl);
-        case 2: return launch_res<2>(partials, TP, residual, gamma, out, residual_out, M, eps, stream, pdl);
-        case 4: return launch_res<4>(partials, TP, residual, gamma, out, residual_out, M, eps, stream, pdl);
-        case 8: return launch_res<8>(partials, TP, residual, gamma, out, residual_out, M, eps, stream, pdl);
-        default: return cudaErrorInvalidValue;
-    }
+    const SplitKPartials none = {};
+    return launch_any<false>(partials, TP, residual, gamma, out, residual_out, M, eps,
+                             ctas_per_row, stream, pdl, none);
+}
+
+cudaError_t launch_reduce_rmsnorm_splitk(void *partials, int TP, const void *residual,
+                                         const void *gamma, void *out, void *residual_out, int M,
+                                         float eps, int ctas_per_row, const SplitKPartials &fix,
+                                         cudaStream_t stream, bool pdl) {
+    return launch_any<true>(partials, TP, residual, gamma, out, residual_out, M, eps,
+                            ctas_per_row, stream, pdl, fix);
 }
 
 }  // namespace skinny

@@ -141,6 +141,33 @@ def test_reduce_rejects_before_cuda(lib):
     assert f(part, 8, res, gam, out, res + 16, 2, 1e-6, None) == 6     # partial residual overlap
 
 
+def test_fused_rejects_before_cuda(lib):
+    buf = ctypes.create_string_buffer(1 << 23)
+    p = ctypes.addressof(buf) + (-ctypes.addressof(buf)) % 256
+    MB = 1 << 20
+    x, W, part, res, gam, out, rout = p, p + 65536, p + 2 * MB, p + 3 * MB, p + 3 * MB + 65536, \
+        p + 4 * MB, p + 5 * MB
+    f = lib.decode_gemm_bf16_reduce_rmsnorm
+    names = ["x", "W", "part", "TP", "res", "gam", "out", "rout", "M", "K", "eps", "s"]
+    ok = dict(zip(names, (x, W, part, 8, res, gam, out, rout, 2, 64, 1e-6, None)))
+
+    def call(**kw):
+        args = dict(ok)
+        args.update(kw)
+        return f(*[args[n] for n in names])
+    for name in ("x", "W", "part", "gam", "out", "rout"):
+        assert call(**{name: None}) == 1
+    assert call(M=0) == 2 and call(M=65) == 2
+    assert call(TP=0) == 2 and call(TP=9) == 2
+    assert call(K=60) == 2 and call(K=0) == 2
+    assert call(eps=0.0) == 10 and call(eps=float("nan")) == 10
+    assert call(x=x + 8) == 3 and call(part=part + 2) == 3 and call(out=out + 8) == 3
+    assert call(out=rout) == 6                          # out == residual_out
+    assert call(out=part + 256) == 6                    # out over the slots
+    assert call(part=W + 4096) == 6                     # slot 0 written over W
+    assert call(rout=res + 16) == 6                     # partial residual overlap
+
+
 def test_gather_rejects_before_cuda(lib):
     buf = ctypes.create_string_buffer(1 << 20)
     p = ctypes.addressof(buf) + (-ctypes.addressof(buf)) % 256

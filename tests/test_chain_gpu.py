@@ -96,3 +96,24 @@ def test_chain_eager_and_graph_replay_give_the_same_bits(chain_inputs):
     for got in (b_res, g_res):
         assert torch.equal(got.view(torch.int16), a_res.view(torch.int16))
     assert not compare.is_nonfinite(workloads.bits(a_out)).any()
+
+
+def test_fused_chain_equals_unfused_chain(chain_inputs):
+    """The chain with decode_gemm_bf16_reduce_rmsnorm for each layer's second GEMM
+    and reduce gives the unfused chain's rows bit for bit (PDL on)."""
+    inp = chain_inputs
+    rows = []
+    for fused in (False, True):
+        chain = LayerChain(inp.W1, inp.W2, inp.peers, inp.gamma, CFG.M, CFG.eps, fused=fused)
+        chain.x.copy_(inp.x0)
+        chain.res_in.copy_(inp.residual0)
+        prev = sk.set_pdl(True)
+        try:
+            out, res = (t.clone() for t in chain.run())
+            torch.cuda.synchronize()
+        finally:
+            sk.set_pdl(prev)
+        rows.append((out, res))
+    (o0, r0), (o1, r1) = rows
+    assert torch.equal(o0.view(torch.int16), o1.view(torch.int16))
+    assert torch.equal(r0.view(torch.int16), r1.view(torch.int16))
