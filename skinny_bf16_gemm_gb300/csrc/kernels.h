@@ -77,6 +77,11 @@ cudaError_t launch_reduce_rmsnorm(const void *partials, int TP, const void *resi
                                   const void *gamma, void *out, void *residual_out, int M,
                                   float eps, int ctas_per_row, cudaStream_t stream, bool pdl);
 
+// Finish a publish-only decode GEMM: out[M, N] = the partials added in K order,
+// rounded once to BF16.
+cudaError_t launch_splitk_finish(const SplitKPartials &fix, uint16_t *out, cudaStream_t stream,
+                                 bool pdl);
+
 // The same with slot 0 made from a publish-only GEMM's FP32 partials (added in
 // K order, rounded once, and written to slot 0 of `partials`).
 cudaError_t launch_reduce_rmsnorm_splitk(void *partials, int TP, const void *residual,
