@@ -635,63 +635,71 @@ def main():
     traffic = recorded_traffic("chain_gemm")
 
     # ---- end to end through the public API: host inputs in, host result out ----
-    # Two buffer sets (sharing the weights) and a copy stream: step i+1's inputs
-    # go up while step i computes, and step i's result rows come back once it is
-    # done. Every step still copies its own inputs in and its result out inside
-    # the timed region.
+    # Steps go in groups of G, each step with its own buffer set (sharing the
+    # weights), two groups' sets in all, and a copy stream: group k+1's inputs go
+    # up while group k computes, and each step's result rows come back once its
+    # group is done. Every step copies its own inputs in and its rows out inside
+    # the timed region; one event per group (not per step) keeps the compute
+    # stream's kernels chained under programmatic dependent launch.
+    G = 4
     pin = dict(pin_memory=True)
     host_x = inp.x0.cpu().pin_memory()
     host_res = inp.residual0.cpu().pin_memory()
     host_peers = [p.cpu().pin_memory() for p in inp.peers]
-    host_out = [torch.empty(cfg.M, cfg.hidden, dtype=torch.bfloat16, **pin) for _ in range(2)]
-    host_res_out = [torch.empty(cfg.M, cfg.hidden, dtype=torch.bfloat16, **pin) for _ in range(2)]
+    host_out = [torch.empty(cfg.M, cfg.hidden, dtype=torch.bfloat16, **pin) for _ in range(2 * G)]
+    host_res_out = [torch.empty(cfg.M, cfg.hidden, dtype=torch.bfloat16, **pin) for _ in range(2 * G)]
     h2d = (host_x.numel() + host_res.numel() + sum(p.numel() for p in host_peers)) * 2
     d2h = (host_out[0].numel() + host_res_out[0].numel()) * 2
-    e2e_steps = max(1, min(args.steps, 500))
-    chains = [chain, LayerChain(inp.W1, inp.W2, inp.peers, inp.gamma, cfg.M, cfg.eps, device=device,
-                                fused=bool(args.fused))]
+    e2e_steps = max(G, min(args.steps, 500)) // G * G
+    chains = [chain] + [LayerChain(inp.W1, inp.W2, inp.peers, inp.gamma, cfg.M, cfg.eps,
+                                   device=device, fused=bool(args.fused))
+                        for _ in range(2 * G - 1)]
     copy_stream = torch.cuda.Stream()
     inputs_ready = [torch.cuda.Event() for _ in range(2)]
     done = [torch.cuda.Event() for _ in range(2)]
 
-    def upload(i):
-        c = chains[i % 2]
+    def upload(k):
         with torch.cuda.stream(copy_stream):
-            c.x.copy_(host_x, non_blocking=True)
-            c.res_in.copy_(host_res, non_blocking=True)
-            for l in range(cfg.layers):
-                c.partials[l][1:].copy_(host_peers[l], non_blocking=True)
-            inputs_ready[i % 2].record(copy_stream)
+            for j in range(G):
+                c = chains[(k % 2) * G + j]
+                c.x.copy_(host_x, non_blocking=True)
+                c.res_in.copy_(host_res, non_blocking=True)
+                for l in range(cfg.layers):
+                    c.partials[l][1:].copy_(host_peers[l], non_blocking=True)
+            inputs_ready[k % 2].record(copy_stream)
 
     def e2e_steps_run(n):
+        groups = n // G
         upload(0)
-        for i in range(n):
-            c = chains[i % 2]
-            stream.wait_event(inputs_ready[i % 2])
-            out, res = c.run()
-            done[i % 2].record(stream)
+        last = None
+        for k in range(groups):
+            stream.wait_event(inputs_ready[k % 2])
+            rows = [chains[(k % 2) * G + j].run() for j in range(G)]
+            done[k % 2].record(stream)
             with torch.cuda.stream(copy_stream):
-                if i + 1 < n:
-                    if i >= 1:  # the other buffer set's last step must be done
-                        copy_stream.wait_event(done[(i + 1) % 2])
-                    upload(i + 1)
-                copy_stream.wait_event(done[i % 2])
-                host_out[i % 2].copy_(out, non_blocking=True)
-                host_res_out[i % 2].copy_(res, non_blocking=True)
+                if k + 1 < groups:
+                    if k >= 1:  # the other group's buffer sets must be free
+                        copy_stream.wait_event(done[(k + 1) % 2])
+                    upload(k + 1)
+                copy_stream.wait_event(done[k % 2])
+                for j, (out, res) in enumerate(rows):
+                    host_out[(k % 2) * G + j].copy_(out, non_blocking=True)
+                    host_res_out[(k % 2) * G + j].copy_(res, non_blocking=True)
+            last = (k % 2) * G + G - 1
         stream.wait_stream(copy_stream)
+        return last
 
-    e2e_steps_run(3)
+    e2e_steps_run(2 * G)
     torch.cuda.synchronize()
     barrier()
     e0.record(stream)
-    e2e_steps_run(e2e_steps)
+    last = e2e_steps_run(e2e_steps)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     # Every step has the same inputs: the rows read back must be the device path's.
     ref_out, ref_res = chain.run()
     torch.cuda.synchronize()
-    last = (e2e_steps - 1) % 2
     if not (torch.equal(host_out[last].view(torch.int16), ref_out.cpu().view(torch.int16)) and
             torch.equal(host_res_out[last].view(torch.int16), ref_res.cpu().view(torch.int16))):
         raise RuntimeError("end-to-end result rows differ from the device-resident run")
