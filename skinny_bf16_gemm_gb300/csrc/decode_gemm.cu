@@ -317,7 +317,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // is free. Wait until the other contributors have published their
         // partials, pull them into the ring with bulk copies (all in flight at
         // once), add in K (= CTA) order and round once. false = aborted.
-        auto finish_tile = [&](int t, int first, int last, const float *own) -> bool {
+        auto finish_tile = [&](int t, int first, int last, const float *own,
+                               int first_peer_slot) -> bool {
             float sum[MP];
 #pragma unroll
             for (int m = 0; m < MP; ++m) sum[m] = own[m];
@@ -331,9 +332,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::mbar_arrive_expect_tx(bar_fix, static_cast<uint32_t>(n_in * slot_bytes));
                 fix_pending = true;
                 int r = kWaitDone;
+                int slot = 0;
                 if (etid < n_in) {
                     const int c = c0 + etid;
-                    const unsigned *flag = args.flags + partial_slot(g, c, t);
+                    slot = c0 == first + 1 ? first_peer_slot : partial_slot(g, c, t);
+                    const unsigned *flag = args.flags + slot;
                     if (ptx::ld_relaxed_gpu(flag) == 0u) {
                         const uint64_t t0 = ptx::global_timer_ns();
                         for (uint32_t spin = 1; ptx::ld_relaxed_gpu(flag) == 0u; ++spin) {
@@ -347,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         __threadfence();                  // acquire the partial behind the flag
                         ptx::fence_proxy_async_global();  // ... for the bulk copy that reads it
                         ptx::bulk_load(sbase + etid * slot_bytes,
-                                       args.partials + static_cast<size_t>(partial_slot(g, c, t)) * args.slot_floats,
+                                       args.partials + static_cast<size_t>(slot) * args.slot_floats,
                                        slot_bytes, bar_fix);
                     }
                 }
@@ -365,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (m < g.M) sum[m] = __fadd_rn(sum[m], src[m * kBlockN]);
                 }
                 // The partials are consumed: re-arm their flags for the next call.
-                if (etid < n_in) args.flags[partial_slot(g, c0 + etid, t)] = 0u;
+                if (etid < n_in) args.flags[slot] = 0u;
                 ptx::named_barrier_sync(1, kEpilogueThreads);  // the ring is refilled next
                 c0 = c1;
             }
@@ -381,6 +384,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         for (int q = 0; q < pieces; ++q) {
             const Piece p = cta_piece(g, cta, q);
+            // The plan's arithmetic (64-bit divisions) before the wait, not on
+            // the split-K tail after it.
+            int first, last;
+            tile_contributors(g, p.tile, first, last);
+            const int my_slot = partial_slot(g, cta, p.tile);
+            const int first_peer_slot =
+                first + 1 + etid <= last ? partial_slot(g, first + 1 + etid, p.tile) : 0;
             const int b = q & 1;
             const uint32_t aph = (q >> 1) & 1;
             const int r = bounded_wait(bar_acc_full + 8 * b, aph, abort_flag, limit);
@@ -415,17 +425,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 continue;
             }
-            int first, last;
-            tile_contributors(g, p.tile, first, last);
             if (first == cta && !args.publish_only) {
                 // The tile starts in this CTA's range: this CTA finishes it.
-                if (!finish_tile(p.tile, first, last, acc)) break;
+                if (!finish_tile(p.tile, first, last, acc, first_peer_slot)) break;
                 continue;
             }
             // Publish this CTA's partial: the values, then a release flag. The
             // finishing CTA reads them with bulk copies (the async proxy).
-            float *mine =
-                args.partials + static_cast<size_t>(partial_slot(g, cta, p.tile)) * args.slot_floats;
+            float *mine = args.partials + static_cast<size_t>(my_slot) * args.slot_floats;
 #pragma unroll
             for (int m = 0; m < MP; ++m)
                 if (m < g.M) __stcg(mine + m * kBlockN + row, acc[m]);
@@ -436,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // stores of the partial.
             if (etid == 0) {
                 __threadfence();
-                ptx::st_release_gpu(args.flags + partial_slot(g, cta, p.tile), 1u);
+                ptx::st_release_gpu(args.flags + my_slot, 1u);
             }
         }
         if (fix_pending) {
