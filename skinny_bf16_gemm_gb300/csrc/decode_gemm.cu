@@ -337,9 +337,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int c = c0 + etid;
                     slot = c0 == first + 1 ? first_peer_slot : partial_slot(g, c, t);
                     const unsigned *flag = args.flags + slot;
-                    if (ptx::ld_relaxed_gpu(flag) == 0u) {
+                    // Acquire loads: the partial behind the flag is visible once it is 1.
+                    if (ptx::ld_acquire_gpu(flag) == 0u) {
                         const uint64_t t0 = ptx::global_timer_ns();
-                        for (uint32_t spin = 1; ptx::ld_relaxed_gpu(flag) == 0u; ++spin) {
+                        for (uint32_t spin = 1; ptx::ld_acquire_gpu(flag) == 0u; ++spin) {
                             if ((spin & 15u) == 0) {
                                 if (*abort_flag) { r = kWaitAborted; break; }
                                 if (ptx::global_timer_ns() - t0 > limit) { r = kWaitTimeout; break; }
@@ -347,8 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                     if (r == kWaitDone) {
-                        __threadfence();                  // acquire the partial behind the flag
-                        ptx::fence_proxy_async_global();  // ... for the bulk copy that reads it
+                        ptx::fence_proxy_async_global();  // the bulk copy reads what was acquired
                         ptx::bulk_load(sbase + etid * slot_bytes,
                                        args.partials + static_cast<size_t>(slot) * args.slot_floats,
                                        slot_bytes, bar_fix);
@@ -439,10 +439,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (args.publish_only) continue;  // read by the next kernel, after this grid
             ptx::fence_proxy_async_global();
             ptx::named_barrier_sync(1, kEpilogueThreads);
-            // One release (fence + store) after the barrier covers every thread's
-            // stores of the partial.
+            // One release store after the barrier covers every thread's stores of
+            // the partial (the barrier orders them before it).
             if (etid == 0) {
-                __threadfence();
                 ptx::st_release_gpu(args.flags + my_slot, 1u);
             }
         }

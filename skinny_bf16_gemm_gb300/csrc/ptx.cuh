@@ -202,9 +202,9 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {
 
 // ---- global memory ---------------------------------------------------------------
 
-__device__ __forceinline__ unsigned ld_relaxed_gpu(const unsigned *p) {
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p) {
     unsigned v;
-    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
 
