@@ -50,6 +50,9 @@ def parse():
     ap.add_argument("--fused", type=int, default=1,
                     help="each layer's second GEMM and reduce + RMSNorm through "
                          "decode_gemm_bf16_reduce_rmsnorm (bit-identical; 0: the two calls)")
+    ap.add_argument("--l2-prefetch", type=int, default=0,
+                    help="weight blocks each decode GEMM CTA (deep ring) prefetches to L2 "
+                         "before its PDL wait, in the chain (library default 6)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true",
                     help="per-config GB/s of every GEMM and reduce config instead of the chain")
@@ -466,11 +469,13 @@ def run_profile_configs(args):
 
 def run_profile(args):
     """Three launches each of the chain's two decode GEMMs and its reduce, on the
-    chain's shapes (weights 264 MB each, larger than L2), for ncu captures."""
+    chain's shapes (weights 264 MB each, larger than L2), PDL and L2 lead as the
+    chain runs them, for ncu captures."""
     import __graft_entry__
     __graft_entry__.build()
     import skinny_bf16_gemm_gb300 as sk
     sk.set_pdl(bool(args.pdl))
+    sk.set_l2_prefetch(args.l2_prefetch)
     cfg = workloads.CHAIN
     dev = torch.device("cuda", 0)
     g1, g2 = cfg.gemm1(), cfg.gemm2()
@@ -523,7 +528,7 @@ def main():
     from skinny_bf16_gemm_gb300.replicas import replica_seed
     inp = workloads.chain_inputs(cfg, replica_seed(workloads.seed_for("chain"), rank), device=device)
     chain = LayerChain(inp.W1, inp.W2, inp.peers, inp.gamma, cfg.M, cfg.eps, device=device,
-                       fused=bool(args.fused))
+                       fused=bool(args.fused), l2_prefetch=args.l2_prefetch)
     chain.x.copy_(inp.x0)
     chain.res_in.copy_(inp.residual0)
     sk.set_pdl(bool(args.pdl))
@@ -625,7 +630,11 @@ def main():
         return e0.elapsed_time(e1)
 
     gemm_launches = kernel_steps * 2 * cfg.layers
-    gemm_ms = loop_ms(gemm_only, kernel_steps) / gemm_launches
+    prev_lead = sk.set_l2_prefetch(args.l2_prefetch)  # as the chain runs its GEMMs
+    try:
+        gemm_ms = loop_ms(gemm_only, kernel_steps) / gemm_launches
+    finally:
+        sk.set_l2_prefetch(prev_lead)
     reduce_reps = 100
     reduce_ms = graph_ms(reduce_only, reduce_reps) / (reduce_reps * cfg.layers)
     g1 = cfg.gemm1()
@@ -652,7 +661,8 @@ def main():
     d2h = (host_out[0].numel() + host_res_out[0].numel()) * 2
     e2e_steps = max(G, min(args.steps, 500)) // G * G
     chains = [chain] + [LayerChain(inp.W1, inp.W2, inp.peers, inp.gamma, cfg.M, cfg.eps,
-                                   device=device, fused=bool(args.fused))
+                                   device=device, fused=bool(args.fused),
+                                   l2_prefetch=args.l2_prefetch)
                         for _ in range(2 * G - 1)]
     copy_stream = torch.cuda.Stream()
     inputs_ready = [torch.cuda.Event() for _ in range(2)]
@@ -713,6 +723,7 @@ def main():
         "impl": "ours",
         "config": workload_config(cfg, {"pdl": bool(args.pdl), "graph": bool(args.graph),
                                         "fused_gemm_reduce": bool(args.fused),
+                                        "l2_prefetch_blocks": args.l2_prefetch,
                                         "parallelism": "replicas" if world > 1 else "single"}),
         "hbm_frac_of_measured": value / peak,
         "hbm_frac_of_nominal_8000": value / 8000.0,
@@ -724,7 +735,7 @@ def main():
                      "algorithmic_bytes_per_launch": gemm_bytes,
                      "avg_launch_ms": gemm_ms, "launches_timed": gemm_launches,
                      "timing": "back-to-back launches of the chain's 6 GEMMs (decode_gemm_bf16), "
-                               "CUDA events around the loop, PDL as in the timed region"},
+                               "CUDA events around the loop, PDL and L2 lead as in the timed region"},
         "kernels": {"decode_gemm_avg_us": gemm_ms * 1e3, "reduce_rmsnorm_avg_us": reduce_ms * 1e3,
                     "reduce_algorithmic_bytes": cfg.reduce().algorithmic_bytes(),
                     "reduce_gbs": cfg.reduce().algorithmic_bytes() / (reduce_ms * 1e-3) / 1e9},

@@ -260,6 +260,21 @@ SKINNY_API int skinny_device_error(int device, int *word);
  */
 SKINNY_API int skinny_set_pdl(int enable);
 
+/*
+ * skinny_set_l2_prefetch -- L2 lead of decode_gemm_bf16's deep ring, for later
+ *   launches of every decode GEMM entry point. With PDL on, each CTA streams its
+ *   first ring of weight tiles and prefetches `blocks` more 16 KB weight blocks
+ *   into L2 before it waits for its predecessor (rings of 9 to 11 stages, used
+ *   when a CTA streams at least 1 MiB; the shallow ring keeps its own lead). A
+ *   performance hint only: results are the same bits for every value. Measured
+ *   on GB300: the default 6 suits a GEMM that follows another GEMM; 0 suits the
+ *   layer chain, where each GEMM follows a short kernel (the reduce) or is
+ *   followed by one, and early requests only slow the previous GEMM's last
+ *   CTAs. blocks in [0, 64]. Returns the previous value, or -1 (setting
+ *   unchanged) if blocks is out of range.
+ */
+SKINNY_API int skinny_set_l2_prefetch(int blocks);
+
 /* ---- host-side planning (no GPU needed) ------------------------------------ */
 
 /* How decode_gemm_bf16 splits a problem over `num_sms` CTAs: one whole 128-row

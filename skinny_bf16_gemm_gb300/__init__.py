@@ -71,6 +71,8 @@ def load_library(path: str = LIBRARY):
     lib.skinny_device_error.restype = i32
     lib.skinny_set_pdl.argtypes = [i32]
     lib.skinny_set_pdl.restype = i32
+    lib.skinny_set_l2_prefetch.argtypes = [i32]
+    lib.skinny_set_l2_prefetch.restype = i32
     lib.skinny_gemm_plan_query.argtypes = [i32, i32, i32, i32, ctypes.POINTER(GemmPlan)]
     lib.skinny_gemm_plan_query.restype = i32
     ip = ctypes.POINTER(i32)
@@ -230,6 +232,15 @@ def device_error(device=None):
 def set_pdl(enable: bool) -> bool:
     """Enable or disable programmatic dependent launch; returns the old setting."""
     return bool(load_library().skinny_set_pdl(1 if enable else 0))
+
+
+def set_l2_prefetch(blocks: int) -> int:
+    """Weight blocks the decode GEMM's deep ring prefetches to L2 before its PDL
+    wait (skinny_set_l2_prefetch); returns the old value."""
+    prev = load_library().skinny_set_l2_prefetch(int(blocks))
+    if prev < 0:
+        raise ValueError(f"l2 prefetch blocks must be in [0, 64], got {blocks}")
+    return prev
 
 
 def gemm_plan(M, N, K, num_sms) -> GemmPlan:

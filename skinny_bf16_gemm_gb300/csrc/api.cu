@@ -34,6 +34,7 @@ struct DeviceState {
 std::mutex g_mutex;
 DeviceState g_devices[kMaxDevices];
 bool g_pdl = false;  // programmatic dependent launch, opt-in (skinny_set_pdl)
+int g_l2_lead = kL2LeadDefault;  // decode GEMM deep-ring L2 lead (skinny_set_l2_prefetch)
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                    const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
@@ -208,6 +209,7 @@ int gemm_launch(const void *x, const void *W, void *out, int M, int N, int K, vo
     {
         std::lock_guard<std::mutex> lock(g_mutex);
         pdl = g_pdl;
+        a.l2_lead = g_l2_lead;
     }
     // Split tiles of 64-row accumulators, every CTA within at most two tiles (two
     // scratch slots), plain output: the GEMM only publishes its partials and a
@@ -309,6 +311,7 @@ int gemm_launch_static(const void *x, const void *W, void *out, int M, int N, in
     {
         std::lock_guard<std::mutex> lock(g_mutex);
         pdl = g_pdl;
+        a.l2_lead = g_l2_lead;
     }
     cudaError_t e = launch_decode_gemm(w_map, x_map, a, mma_n, g.ctas, s, pdl,
                                        use_shallow_ring(g, pdl), dev);
@@ -392,9 +395,11 @@ int decode_gemm_bf16_reduce_rmsnorm(const void *x, const void *W, void *partials
     if ((st = encode_2d(enc, &w_map, W, N, K, kBlockN))) return st;
     if ((st = encode_2d(enc, &x_map, x, M, K, mma_n))) return st;
     bool pdl;
+    int l2_lead;
     {
         std::lock_guard<std::mutex> lock(g_mutex);
         pdl = g_pdl;
+        l2_lead = g_l2_lead;
     }
     GemmArgs a = {};
     a.M = M;
@@ -408,6 +413,7 @@ int decode_gemm_bf16_reduce_rmsnorm(const void *x, const void *W, void *partials
     a.wait_limit_ns = kWaitLimitNs;
     a.scale = 1.0f;
     a.publish_only = 1;
+    a.l2_lead = l2_lead;
     if (launch_decode_gemm(w_map, x_map, a, mma_n, g.ctas, s, pdl, use_shallow_ring(g, pdl), dev) !=
         cudaSuccess) {
         cudaGetLastError();
@@ -573,6 +579,14 @@ int skinny_set_pdl(int enable) {
     std::lock_guard<std::mutex> lock(g_mutex);
     const int prev = g_pdl ? 1 : 0;
     g_pdl = enable != 0;
+    return prev;
+}
+
+int skinny_set_l2_prefetch(int blocks) {
+    if (blocks < 0 || blocks > kL2LeadMax) return -1;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    const int prev = g_l2_lead;
+    g_l2_lead = blocks;
     return prev;
 }
 

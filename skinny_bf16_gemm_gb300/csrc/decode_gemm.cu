@@ -48,8 +48,9 @@ constexpr uint64_t kDrainLimitNs = 200000000ull;  // 0.2 s for copies already is
 // Weight blocks prefetched to L2, beyond the ring's first fill, before waiting
 // on the previous kernel: with the shallow ring (short streams) most of the
 // CTA's range, so the stream runs from L2 once the wait is over; with the deep
-// ring a short lead (a longer one slows the previous kernel's last CTAs).
-constexpr int kL2PrefetchShallow = 26, kL2PrefetchDeep = 6;
+// ring the caller's GemmArgs::l2_lead, a short lead (a longer one slows the
+// previous kernel's last CTAs).
+constexpr int kL2PrefetchShallow = 26;
 constexpr int kMaxShallowStages = 6;  // shallow rings have 4..6 stages, deep ones 9..11
 
 // MP: padded row count (MMA N). STAGES: shared-memory ring depth. The deep ring
@@ -208,7 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tma_load_2d(st, &w_map, bar_full + 8 * j, kb * kBlockK, t * kBlockN, pol_w);
             }
             // The blocks after the ring's worth go to L2 ahead of time.
-            const long long lead = STAGES <= kMaxShallowStages ? kL2PrefetchShallow : kL2PrefetchDeep;
+            const long long lead = STAGES <= kMaxShallowStages ? kL2PrefetchShallow : args.l2_lead;
             const long long npf = total - npre < lead ? total - npre : lead;
             for (long long j = npre; j < npre + npf; ++j) {
                 const long long blk = b0 + j;

@@ -34,7 +34,17 @@ struct GemmArgs {
     // slot and nothing is finished here (no flags): the reduce kernel that follows
     // adds them (decode_gemm_bf16_reduce_rmsnorm).
     int publish_only;
+    // Deep ring only: weight blocks each CTA prefetches into L2, beyond its ring's
+    // first fill, before waiting on the previous kernel (skinny_set_l2_prefetch).
+    int l2_lead;
 };
+
+// Default and largest l2_lead. Measured on GB300: 6 suits back-to-back GEMMs
+// (each CTA's early blocks arrive while the previous kernel's last CTAs finish);
+// 0 suits a GEMM behind a short latency-bound kernel, such as the layer chain's
+// reduce, where those requests only slow the previous GEMM's last CTAs.
+constexpr int kL2LeadDefault = 6;
+constexpr int kL2LeadMax = 64;
 
 // Where the reduce kernel finds a publish-only GEMM's partials of the 7168
 // slot-0 columns: the GEMM's geometry (tiles, K blocks, CTAs) and scratch.

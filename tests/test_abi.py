@@ -274,3 +274,33 @@ def test_work_split_covers_every_block_once(lib, M, N, K, sms):
         if len(cs) > 1:
             firsts.append(cs[0])
     assert len(firsts) == len(set(firsts)) == plan.split_tiles
+
+
+def test_l2_prefetch_setting_round_trips_and_rejects_out_of_range(lib):
+    """skinny_set_l2_prefetch returns the previous lead, accepts [0, 64] and
+    leaves the setting unchanged (returning -1) outside it."""
+    prev = lib.skinny_set_l2_prefetch(0)
+    try:
+        assert 0 <= prev <= 64
+        assert lib.skinny_set_l2_prefetch(64) == 0
+        assert lib.skinny_set_l2_prefetch(-1) == -1
+        assert lib.skinny_set_l2_prefetch(65) == -1
+        assert lib.skinny_set_l2_prefetch(6) == 64
+        with pytest.raises(ValueError):
+            sk.set_l2_prefetch(100)
+        assert sk.set_l2_prefetch(3) == 6
+    finally:
+        lib.skinny_set_l2_prefetch(prev)
+
+
+def test_default_l2_prefetch_is_six(lib):
+    prev = lib.skinny_set_l2_prefetch(6)
+    lib.skinny_set_l2_prefetch(prev)
+    # A fresh process starts at the library default.
+    import subprocess, sys
+    code = ("import skinny_bf16_gemm_gb300 as sk; lib = sk.load_library(); "
+            "print(lib.skinny_set_l2_prefetch(0))")
+    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True,
+                         cwd=os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    assert out.returncode == 0, out.stderr
+    assert out.stdout.strip() == "6"

@@ -100,20 +100,25 @@ def test_chain_eager_and_graph_replay_give_the_same_bits(chain_inputs):
 
 def test_fused_chain_equals_unfused_chain(chain_inputs):
     """The chain with decode_gemm_bf16_reduce_rmsnorm for each layer's second GEMM
-    and reduce gives the unfused chain's rows bit for bit (PDL on)."""
+    and reduce gives the unfused chain's rows bit for bit (PDL on), whatever the
+    decode GEMM's L2 lead; the chain puts the caller's lead back after a step."""
     inp = chain_inputs
     rows = []
-    for fused in (False, True):
-        chain = LayerChain(inp.W1, inp.W2, inp.peers, inp.gamma, CFG.M, CFG.eps, fused=fused)
+    for fused, lead in ((False, 6), (True, 0), (True, 6), (False, 0)):
+        chain = LayerChain(inp.W1, inp.W2, inp.peers, inp.gamma, CFG.M, CFG.eps, fused=fused,
+                           l2_prefetch=lead)
         chain.x.copy_(inp.x0)
         chain.res_in.copy_(inp.residual0)
         prev = sk.set_pdl(True)
+        prev_lead = sk.set_l2_prefetch(9)
         try:
             out, res = (t.clone() for t in chain.run())
             torch.cuda.synchronize()
+            assert sk.set_l2_prefetch(prev_lead) == 9
         finally:
             sk.set_pdl(prev)
         rows.append((out, res))
-    (o0, r0), (o1, r1) = rows
-    assert torch.equal(o0.view(torch.int16), o1.view(torch.int16))
-    assert torch.equal(r0.view(torch.int16), r1.view(torch.int16))
+    o0, r0 = rows[0]
+    for o1, r1 in rows[1:]:
+        assert torch.equal(o0.view(torch.int16), o1.view(torch.int16))
+        assert torch.equal(r0.view(torch.int16), r1.view(torch.int16))

@@ -161,3 +161,26 @@ def test_gemm_with_pdl_matches(cuda_ok):
         sk.set_pdl(prev)
     for o in outs:
         assert torch.equal(o.view(torch.int16), base.view(torch.int16))
+
+
+@pytest.mark.parametrize("M,N,K", [(16, 12288, 7168), (64, 7168, 14336), (1, 20480, 7168)])
+def test_gemm_l2_lead_changes_no_bits(cuda_ok, M, N, K):
+    """The deep ring's L2 lead (skinny_set_l2_prefetch) is a scheduling hint:
+    every value gives the same bits, back to back under PDL, and the result
+    holds against the oracle on sampled columns."""
+    x, W = gemm_inputs_device(M, N, K, 77)
+    prev_pdl = sk.set_pdl(True)
+    prev_lead = sk.set_l2_prefetch(6)
+    try:
+        assert not sk.gemm_plan(M, N, K, torch.cuda.get_device_properties(0).multi_processor_count
+                                ).stages <= 6, "shape must take the deep ring"
+        base = run_gemm(x, W)
+        for lead in (0, 1, 17, 64):
+            sk.set_l2_prefetch(lead)
+            outs = [run_gemm(x, W) for _ in range(2)]
+            for o in outs:
+                assert torch.equal(o.view(torch.int16), base.view(torch.int16)), lead
+    finally:
+        sk.set_l2_prefetch(prev_lead)
+        sk.set_pdl(prev_pdl)
+    check_gemm_sampled(x, W, base, sample_columns(N, count=256, seed=M))
