@@ -46,11 +46,13 @@ constexpr int kEpilogueThreads = 128;
 constexpr int kWBytes = kBlockN * kBlockK * 2;
 constexpr uint64_t kDrainLimitNs = 200000000ull;  // 0.2 s for copies already issued
 // Weight blocks prefetched to L2, beyond the ring's first fill, before waiting
-// on the previous kernel: with the shallow ring (short streams) most of the
-// CTA's range, so the stream runs from L2 once the wait is over; with the deep
-// ring the caller's GemmArgs::l2_lead, a short lead (a longer one slows the
-// previous kernel's last CTAs).
-constexpr int kL2PrefetchShallow = 26;
+// on the previous kernel: 8 with the shallow ring, the caller's GemmArgs::l2_lead
+// with the deep ring. Both short: the early requests share the SM and HBM with
+// the previous kernel's last CTAs and slow them. Measured on GB300 for the
+// shallow ring (its co-resident CTA is the previous kernel's): leads of 8-10
+// beat 26 (most of a short range) by up to 1.4 us at N = 4096 and 3.5 us at
+// N = 6144-7168 (K = 7168, 0.4-0.7 MB per CTA); 0-4 are slower again.
+constexpr int kL2PrefetchShallow = 8;
 constexpr int kMaxShallowStages = 6;  // shallow rings have 4..6 stages, deep ones 9..11
 
 // MP: padded row count (MMA N). STAGES: shared-memory ring depth. The deep ring
