@@ -265,8 +265,8 @@ SKINNY_API int skinny_set_pdl(int enable);
  *   launches of every decode GEMM entry point. With PDL on, each CTA streams its
  *   first ring of weight tiles and prefetches `blocks` more 16 KB weight blocks
  *   into L2 before it waits for its predecessor (rings of 9 to 11 stages, used
- *   when a CTA streams at least 1 MiB, 1.5 MiB for M <= 16; the shallow ring
- *   keeps its own lead). A performance hint only: results are the same bits
+ *   when M > 32 or a CTA streams at least 1 MiB, 1.5 MiB for M <= 16; the
+ *   shallow ring keeps its own lead). A performance hint only: results are the same bits
  *   for every value. Measured
  *   on GB300: the default 6 suits a GEMM that follows another GEMM; 0 suits the
  *   layer chain, where each GEMM follows a short kernel (the reduce) or is
@@ -283,8 +283,8 @@ SKINNY_API int skinny_set_l2_prefetch(int blocks);
  * stream-K: the ceil(N/128) x ceil(K/64) weight blocks, in tile-major order, are
  * cut into `ctas` contiguous, equal-as-possible ranges. The ring depth follows
  * the weight bytes per CTA under the current PDL setting: the shallow ring (two
- * CTAs per SM) below 1 MiB (1.5 MiB for M <= 16) with PDL on, the deep ring
- * otherwise. */
+ * CTAs per SM) below 1 MiB (1.5 MiB for M <= 16) with PDL on and M <= 32, the
+ * deep ring otherwise. */
 typedef struct {
     int tiles;          /* ceil(N / 128): 128-row weight tiles */
     int kblocks;        /* ceil(K / 64): 64-wide K blocks per tile */

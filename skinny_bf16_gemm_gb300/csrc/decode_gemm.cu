@@ -53,7 +53,7 @@ constexpr uint64_t kDrainLimitNs = 200000000ull;  // 0.2 s for copies already is
 // beat 26 (most of a short range) by up to 1.4 us at N = 4096 and 3.5 us at
 // N = 6144-7168 (K = 7168, 0.4-0.7 MB per CTA); 0-4 are slower again.
 constexpr int kL2PrefetchShallow = 8;
-constexpr int kMaxShallowStages = 6;  // shallow rings have 4..6 stages, deep ones 9..11
+constexpr int kMaxShallowStages = 6;  // shallow rings have 5..6 stages, deep ones 9..11
 
 // MP: padded row count (MMA N). STAGES: shared-memory ring depth. The deep ring
 // (185-227 KB) keeps the most bytes in flight; the shallow one (~100-112 KB) lets
@@ -526,15 +526,17 @@ cudaError_t launch_variant(const CUtensorMap &w_map, const CUtensorMap &x_map,
 // 64 rows (their x slices take a larger share of each stage). Measured on GB300:
 // 12 stages for 16 rows gain alone but lose inside the layer chain.
 constexpr int kDeepStages16 = 10, kDeepStages32 = 11, kDeepStages64 = 9;
-// Shallow rings sized so two CTAs fit on one SM (about 112, 104 and 100 KB).
-constexpr int kShallowStages16 = 6, kShallowStages32 = 5, kShallowStages64 = 4;
+// Shallow rings sized so two CTAs fit on one SM (about 112 and 104 KB). Rows of
+// x above 32 always take the deep ring (plan.cuh): a 4-stage shallow ring for
+// them measured 0.6-1 us slower on GB300 even on short streams.
+constexpr int kShallowStages16 = 6, kShallowStages32 = 5;
 static_assert(kShallowStages16 <= kMaxShallowStages && kDeepStages64 > kMaxShallowStages,
               "ring classes must stay apart");
 
 }  // namespace
 
 int gemm_stages(int mma_n, bool shallow) {
-    if (mma_n == 64) return shallow ? kShallowStages64 : kDeepStages64;
+    if (mma_n == 64) return kDeepStages64;
     if (shallow) return mma_n == 16 ? kShallowStages16 : kShallowStages32;
     return mma_n == 16 ? kDeepStages16 : kDeepStages32;
 }
@@ -544,7 +546,7 @@ int gemm_smem_bytes(int mma_n, bool shallow) {
         return shallow ? Layout<16, kShallowStages16>::kDynamicBytes : Layout<16, kDeepStages16>::kDynamicBytes;
     if (mma_n == 32)
         return shallow ? Layout<32, kShallowStages32>::kDynamicBytes : Layout<32, kDeepStages32>::kDynamicBytes;
-    return shallow ? Layout<64, kShallowStages64>::kDynamicBytes : Layout<64, kDeepStages64>::kDynamicBytes;
+    return Layout<64, kDeepStages64>::kDynamicBytes;
 }
 
 cudaError_t launch_decode_gemm(const CUtensorMap &w_map, const CUtensorMap &x_map,
@@ -558,7 +560,6 @@ cudaError_t launch_decode_gemm(const CUtensorMap &w_map, const CUtensorMap &x_ma
         if (shallow) return launch_variant<32, kShallowStages32>(w_map, x_map, args, ctas, stream, pdl, device);
         return launch_variant<32, kDeepStages32>(w_map, x_map, args, ctas, stream, pdl, device);
     }
-    if (shallow) return launch_variant<64, kShallowStages64>(w_map, x_map, args, ctas, stream, pdl, device);
     return launch_variant<64, kDeepStages64>(w_map, x_map, args, ctas, stream, pdl, device);
 }
 

@@ -55,12 +55,15 @@ __host__ __device__ inline int choose_ctas(int N, int num_sms) {
 // on GB300 the two cross near 1 MiB of weights per CTA, and near 1.5 MiB for up
 // to 16 rows of x, whose shallow ring is deepest (6 stages): between 1 and 1.5
 // MiB it is 0.3-0.45 us faster there, level for 32 rows, 3.5-5 us slower for 64.
+// More than 32 rows never take it: their shallow ring could hold only 4 stages,
+// and the deep ring was 0.6-1 us faster even at N = 2048-4096.
 constexpr long long kShallowRingMaxBytes = 1ll << 20;
 constexpr long long kShallowRingMaxBytes16 = 3ll << 19;
 
 __host__ __device__ inline bool use_shallow_ring(const GemmGeometry &g, bool pdl) {
     const long long per_cta = g.blocks * (kBlockN * kBlockK * 2) / g.ctas;
-    return pdl && per_cta < (g.M <= 16 ? kShallowRingMaxBytes16 : kShallowRingMaxBytes);
+    return pdl && g.M <= 32 &&
+           per_cta < (g.M <= 16 ? kShallowRingMaxBytes16 : kShallowRingMaxBytes);
 }
 
 // First weight block of CTA c (c = ctas gives the end of the last range).

@@ -205,11 +205,13 @@ SHAPES = [(1, 16, 64, 152), (4, 2048, 7168, 152), (16, 18432, 7168, 152), (16, 1
     (4, 2048, 7168, True), (16, 4096, 7168, True), (32, 4096, 7168, True),
     (16, 12288, 7168, True), (16, 7168, 14336, True), (17, 12288, 7168, False),
     (32, 7168, 14336, False), (16, 18432, 7168, False), (16, 7168, 18432, False),
-    (64, 18432, 7168, False), (64, 7168, 14336, False), (3, 200, 136, True)])
+    (64, 18432, 7168, False), (64, 7168, 14336, False), (3, 200, 136, True),
+    (64, 4096, 7168, False), (33, 2048, 7168, False), (48, 200, 136, False)])
 def test_ring_depth_follows_weight_bytes_per_cta(lib, M, N, K, expect_shallow):
     """With programmatic dependent launch the shallow ring (two CTAs per SM) is
-    taken below 1 MiB of weights per CTA (1.5 MiB for up to 16 rows), the deep
-    ring (more bytes in flight) above; without it always the deep ring."""
+    taken below 1 MiB of weights per CTA (1.5 MiB for up to 16 rows, never for
+    more than 32), the deep ring (more bytes in flight) above; without it always
+    the deep ring."""
     prev = sk.set_pdl(False)
     try:
         deep = sk.gemm_plan(M, N, K, 152)
@@ -218,7 +220,8 @@ def test_ring_depth_follows_weight_bytes_per_cta(lib, M, N, K, expect_shallow):
     finally:
         sk.set_pdl(prev)
     per_cta = plan.blocks * 128 * 64 * 2 / plan.ctas
-    assert (per_cta < (1.5 if M <= 16 else 1) * 2 ** 20) == expect_shallow
+    limit = 0 if M > 32 else (1.5 if M <= 16 else 1) * 2 ** 20
+    assert (per_cta < limit) == expect_shallow
     if expect_shallow:
         assert plan.stages < deep.stages
         assert 2 * (plan.smem_bytes + 1024) <= 233472  # two CTAs fit on an SM
