@@ -201,6 +201,22 @@ SHAPES = [(1, 16, 64, 152), (4, 2048, 7168, 152), (16, 18432, 7168, 152), (16, 1
           (3, 40000, 1000, 152)]
 
 
+def _random_shapes(count, seed=20261202):
+    # Seeded shapes across the accepted range: any M in 1..64, any N, K a
+    # multiple of 8, and SM counts from tiny to a full GB300.
+    import random
+    r = random.Random(seed)
+    out = []
+    for _ in range(count):
+        out.append((r.randint(1, 64), r.choice([r.randint(1, 300), r.randint(1, 30000)]),
+                    8 * r.choice([r.randint(1, 40), r.randint(1, 2600)]),
+                    r.choice([1, 3, 7, 64, 148, 152])))
+    return out
+
+
+SHAPES += _random_shapes(40)
+
+
 @pytest.mark.parametrize("M,N,K,expect_shallow", [
     (4, 2048, 7168, True), (16, 4096, 7168, True), (32, 4096, 7168, True),
     (16, 12288, 7168, True), (16, 7168, 14336, True), (17, 12288, 7168, False),
@@ -249,7 +265,7 @@ def test_work_split_covers_every_block_once(lib, M, N, K, sms):
     contributors = {}
     slots = set()
     for c in range(plan.ctas):
-        pieces = sk.gemm_cta_pieces(M, N, K, sms, c)
+        pieces = sk.gemm_cta_pieces(M, N, K, sms, c, max_pieces=plan.tiles + 1)
         assert pieces, f"CTA {c} has no work"
         n_blocks = 0
         for (t, kb0, kb1, slot) in pieces:
