@@ -67,8 +67,14 @@ def check_gemm_sampled(x, W, out, cols):
 
 
 def sample_columns(N, count=384, seed=0):
-    """Columns spread over every tile, always including both ends."""
+    """Stratified output columns of an N-column GEMM: in every 128-column tile
+    (one MMA's weight rows) one random column in each 32-column quarter (one
+    epilogue warp's TMEM lanes), plus `count` uniformly random columns and both
+    ends of the first tile and of the matrix."""
     rng = np.random.default_rng(seed)
     base = {0, 1, 127, 128, N - 1, N - 2}
+    for t0 in range(0, N, 128):
+        for q0 in range(t0, min(t0 + 128, N), 32):
+            base.add(int(rng.integers(q0, min(q0 + 32, N))))
     base |= set(int(c) for c in rng.integers(0, N, size=count))
     return np.array(sorted(c for c in base if 0 <= c < N), dtype=np.int32)
