@@ -11,14 +11,15 @@ What each function follows (the vLLM DSpark drafter pages):
 
 * ``decode_gemm`` -- "drafter/linears", module text and ``DraftGemm``:
   out[M,N] = x[M,K] @ weight[N,K]^T, BF16 operands, FP32 accumulation, one BF16
-  rounding, "only the summation order differs" from cuBLAS. Reading: the exact
+  rounding, cuBLAS's arithmetic in any order of additions. Reading: the exact
   product sum (binary64 here) rounded once to BF16, ties to even.
 * ``reduce_residual`` -- "drafter/comm", ``ArNorm`` docstring and kernel, and
   "cutedsl/common/twoshot" ``reduce``: FP32 sum of the TP partials in rank order
   0..TP-1 from slot 0, one BF16 rounding, FP32 add of the residual, one BF16
   rounding. Bit-exact by definition.
-* ``rmsnorm`` -- "drafter/comm" module text ("FP32 sum of squares, rsqrt(sum /
-  7168 + eps), x * rstd * w rounded once") and ``ArNorm.kernel``'s last block.
+* ``rmsnorm`` -- "drafter/comm" module text (a sum of squares in FP32, the
+  reciprocal square root of its mean over 7168 columns plus eps, the product
+  x * rstd * gamma rounded once) and ``ArNorm.kernel``'s last block.
   Evaluated in binary64 and rounded once.
 * ``decode_gemm_logits`` -- "drafter/linears", ``draft_logits``: the lm_head GEMM
   sliced to its first n_out (org_vocab_size) columns, optional tanh soft cap,

@@ -9,7 +9,7 @@
  * Sources (the vLLM API pages for the DSpark drafter):
  *  - "drafter/linears" module text and DraftGemm docstring: out[M,N] = x[M,K] @
  *    weight[N,K]^T with BF16 operands, FP32 accumulation and one BF16 rounding,
- *    "as cuBLAS; only the summation order differs". The oracle takes the plainest
+ *    cuBLAS's arithmetic with the order of the additions left free. The oracle takes the plainest
  *    reading of that: the dot product in FP64 (every BF16 x BF16 product is exact
  *    in FP64), rounded once to BF16 with round-to-nearest-even.
  *  - "drafter/comm" module text, ArNorm docstring and ArNorm.kernel: the TP BF16
@@ -301,7 +301,7 @@ void oracle_rmsnorm_f32_steps(const uint16_t *h, const uint16_t *gamma, uint16_t
 /*
  * out[m][r * S + j] = shards[r][m][j]: every rank's [M, S] shard placed at
  * columns r*S .. r*S + S - 1 of the gathered [M, TP * S] rows ("drafter/comm",
- * Gather docstring and module text: "rank r's at columns r S .."; gather_context
+ * Gather docstring and module text: rank r's shard starts at column r*S; gather_context
  * and gather_logits build [M, TP * S] from [M, S] shards). A byte move: the
  * values are copied unchanged (no sentinel cleaning -- the local slots have no
  * sentinel). shards is [TP, M, S], out is [M, TP * S].

@@ -18,8 +18,8 @@ import numpy as np  # noqa: E402
 
 import oracle  # noqa: E402
 
-# (binary64 input as a hex float, why it is here). The rounding rule is the pages'
-# "one BF16 rounding" (drafter/linears module text; drafter/comm ArNorm), read as
+# (binary64 input as a hex float, why it is here). The pages round to BF16 a single
+# time (drafter/linears module text; drafter/comm ArNorm); the mode is read as
 # IEEE 754 round-to-nearest-even.
 ROUND_INPUTS = [
     ("0x1.0000000000000p+0", "1.0 exactly"),
@@ -80,8 +80,8 @@ REDUCE_INPUTS = [
 def main():
     lines = ["# BF16 rounding cases: binary64 input (hex float) -> BF16 pattern.",
              "# Expected values written by tests/golden/make_golden.py from the oracle;",
-             "# the rule is the pages' 'one BF16 rounding' (drafter/linears module text,",
-             "# drafter/comm ArNorm) read as IEEE 754 round-to-nearest-even.",
+             "# the pages round to BF16 a single time (drafter/linears module text,",
+             "# drafter/comm ArNorm); the mode is read as IEEE 754 round-to-nearest-even.",
              "# input expected  # reason"]
     for text, why in ROUND_INPUTS:
         v = float.fromhex(text)
