@@ -23,14 +23,24 @@
  *    enqueued on it; the call returns without waiting for the GPU.
  *  - Return value: SKINNY_OK (0) or a skinny_status code. On any nonzero code
  *    nothing was launched and no output was touched. Faults of the GPU work
- *    itself surface later, at a stream synchronisation, as CUDA errors; a
- *    kernel whose internal wait ran out instead records a code that
- *    skinny_device_error() returns.
+ *    itself surface later, at a stream synchronisation, as CUDA errors.
+ *  - Every wait inside a decode GEMM kernel is bounded (1 s). A kernel whose
+ *    wait ran out records it in a device error word and in a host-mapped word;
+ *    from then on every call that uses the decode GEMM's scratch on that device
+ *    returns SKINNY_ERR_TIMEOUT without launching, until skinny_device_error()
+ *    reads and clears the error (and re-arms the scratch). The output of the
+ *    kernel that gave up is unspecified.
  *  - Nothing is allocated per call. decode_gemm_bf16 uses a per-device scratch
- *    area (split-K partial sums, published-partial flags, an error word) that its first
- *    call on each device allocates with cudaMalloc; make that first call outside
- *    CUDA stream capture. Calls on one device whose kernels may overlap in time
- *    (unordered streams) share that scratch and must not be issued.
+ *    area (split-K partial sums, published-partial flags, an error word, plus
+ *    one page of host-mapped memory) that its first call on each device
+ *    allocates; make that first call outside CUDA stream capture. All calls on
+ *    one device share that scratch, whatever their stream: calls whose kernels
+ *    may run at the same time (streams not ordered with each other by events or
+ *    a common predecessor) race on it and give wrong results, so order them.
+ *  - Launch settings: programmatic dependent launch and the decode GEMM's L2
+ *    lead are process-wide settings (skinny_set_pdl, skinny_set_l2_prefetch)
+ *    that the _ex entry points override per call (skinny_launch_opts), so code
+ *    that wants its own settings never changes what other threads' calls see.
  *  - Calls are thread-safe on the host.
  */
 #ifndef SKINNY_H
@@ -62,12 +72,12 @@ typedef enum {
     SKINNY_ERR_ARG = 10      /* a scalar argument is invalid (eps, timeout, ...) */
 } skinny_status;
 
-/* Row width of every reduce + RMSNorm row: 7168 ("drafter/comm", ArNorm:
- * "All-reduce of BF16 rows [M, 7168]"; the mean divides by 7168). */
+/* Row width of every reduce + RMSNorm row: 7168 ("drafter/comm", ArNorm
+ * docstring: the all-reduced rows are M x 7168 BF16; the mean divides by 7168). */
 #define SKINNY_HIDDEN 7168
-/* Largest row count of decode_gemm_bf16: the pages' engine serves "up to 32
- * rows" ("drafter/linears" module text); this library also serves 33..64 (the
- * row cap of the pages' reduction buffers, "cutedsl/common/twoshot", cap=64). */
+/* Largest row count of decode_gemm_bf16: the pages' engine keeps its speed for at
+ * most 32 rows ("drafter/linears" module text); this library also serves 33..64
+ * (the row cap of the pages' reduction buffers, "cutedsl/common/twoshot", cap=64). */
 #define SKINNY_GEMM_MAX_M 64
 /* Largest row count of reduce_residual_rmsnorm (the row cap of the pages'
  * reduction buffers, "cutedsl/common/twoshot", TwoShot: cap=64). */
@@ -76,11 +86,21 @@ typedef enum {
  * pages, "drafter/comm" module text). */
 #define SKINNY_REDUCE_MAX_TP 8
 
+/* Per-call launch settings of the _ex entry points. Each field is either a
+ * value or SKINNY_OPT_DEFAULT, which takes the process-wide setting. */
+#define SKINNY_OPT_DEFAULT (-1)
+typedef struct {
+    int pdl;          /* 1: programmatic dependent launch (see skinny_set_pdl), 0: off */
+    int l2_prefetch;  /* decode GEMM deep-ring L2 lead in [0, 64] (see
+                         skinny_set_l2_prefetch); ignored by the reduce */
+} skinny_launch_opts;
+
 /*
  * decode_gemm_bf16 -- out[M,N] = x[M,K] @ W[N,K]^T
- *   ("drafter/linears": module text, "Precision: BF16 operands, FP32
- *    accumulation, one BF16 rounding, as cuBLAS; only the summation order
- *    differs"; DraftGemm: out[M, N] = x[M, K] @ weight[N, K]^T.)
+ *   ("drafter/linears": the module text fixes the precision -- BF16 inputs, an
+ *    FP32 accumulator, a single rounding to BF16, the same arithmetic as cuBLAS
+ *    with the order of the additions free; DraftGemm gives the product
+ *    out[M, N] = x[M, K] @ weight[N, K]^T.)
  *
  *   x    [M, K] BF16, row-major (row stride K elements), 16-byte aligned.
  *   W    [N, K] BF16, row-major (each weight row is one output column), 16-byte
@@ -94,10 +114,20 @@ typedef enum {
  *   CTAs, partial sums added in K order), rounded once to BF16 (nearest even).
  *   Deterministic: the same inputs on the same device give the same bits.
  *   Errors: SKINNY_ERR_NULL, _SHAPE, _ALIGN, _ALIAS, _DEVICE, _CAPTURE, _ALLOC,
- *   _LAUNCH as above.
+ *   _LAUNCH as above; _TIMEOUT while an earlier kernel's wait that ran out is
+ *   not yet cleared (see the conventions at the top).
  */
 SKINNY_API int decode_gemm_bf16(const void *x, const void *W, void *out,
                      int M, int N, int K, void *stream);
+
+/*
+ * decode_gemm_bf16_ex -- decode_gemm_bf16 with per-call launch settings.
+ *   opts: host pointer, or NULL for the process-wide settings. The settings
+ *   change when and how the kernel's work is scheduled, never a result bit.
+ *   Errors: as decode_gemm_bf16, plus SKINNY_ERR_ARG for a field out of range.
+ */
+SKINNY_API int decode_gemm_bf16_ex(const void *x, const void *W, void *out, int M, int N,
+                                   int K, const skinny_launch_opts *opts, void *stream);
 
 /*
  * decode_gemm_bf16_logits -- the lm_head logits with the epilogue fused
@@ -118,14 +148,12 @@ SKINNY_API int decode_gemm_bf16_logits(const void *x, const void *W, void *out, 
 
 /*
  * decode_gemm_bf16_noalloc -- decode_gemm_bf16 that allocates no device memory
- *   The drafter pages have no counterpart to this entry point; it exists for
- *   callers that cannot let a library call cudaMalloc. Examples: code that runs
- *   while a CUDA graph is being captured in the strict capture mode (there
- *   cudaMalloc is an error that also invalidates the capture); serving engines
- *   that give all spare device memory to their own pool at start-up, so any later
- *   allocation fails or evicts cache; plug-ins that may only use their host
- *   framework's allocator; latency-critical loops that cannot afford cudaMalloc's
- *   implicit synchronisation.
+ *   The drafter pages have no counterpart to this entry point. It is for callers
+ *   that cannot let a library call cudaMalloc: serving engines that hand all
+ *   spare device memory to their own pool at start-up, so that a later
+ *   allocation fails or forces the pool to give memory back; plug-ins that may
+ *   only take memory from their host framework's allocator; loops that cannot
+ *   afford cudaMalloc's implicit device synchronisation.
  *
  *   Same arguments, layouts, results and errors as decode_gemm_bf16 (the same
  *   kernel runs). The split-K scratch -- partial tiles, published-partial flags, error
@@ -147,13 +175,15 @@ SKINNY_API int decode_gemm_bf16_noalloc(const void *x, const void *W, void *out,
 
 /*
  * reduce_residual_rmsnorm -- the ArNorm row operation on TP local slots
- *   ("drafter/comm": module text -- "summed in FP32 in rank order 0 .. TP-1 and
- *    rounded once to BF16 ..., the residual is added (one BF16 rounding) and the
- *    RMSNorm of the new residual follows (FP32 sum of squares, rsqrt(sum / 7168
- *    + eps), x * rstd * w rounded once)"; ArNorm docstring for the argument list
- *    and "residual False: the new residual is the all-reduced row itself";
- *    "cutedsl/common/twoshot": owners = 1 as the one-GPU stand-in, TP local slots
- *    playing the ranks.)
+ *   ("drafter/comm": the module text and the ArNorm kernel define the steps --
+ *    the TP partial rows are added in FP32 from rank 0 upwards and rounded to
+ *    BF16 once, the residual is added with a second BF16 rounding, and the
+ *    RMSNorm of that new residual uses an FP32 sum of squares, the reciprocal
+ *    square root of its mean over 7168 columns plus eps, and one rounding of
+ *    x * rstd * gamma; the ArNorm docstring gives the argument list and, when no
+ *    residual is given, makes the summed row itself the new residual.
+ *    "cutedsl/common/twoshot": with a single owner the TP ranks can be local
+ *    slots of one GPU, the stand-in used here.)
  *
  *   partials      [TP, M, 7168] BF16, contiguous (slot r = rank r's partial row),
  *                 16-byte aligned.
@@ -173,6 +203,13 @@ SKINNY_API int decode_gemm_bf16_noalloc(const void *x, const void *W, void *out,
 SKINNY_API int reduce_residual_rmsnorm(const void *partials, int TP, const void *residual,
                             const void *gamma, void *out, void *residual_out,
                             int M, float eps, void *stream);
+
+/* reduce_residual_rmsnorm with per-call launch settings (as decode_gemm_bf16_ex;
+ * only opts->pdl applies). */
+SKINNY_API int reduce_residual_rmsnorm_ex(const void *partials, int TP, const void *residual,
+                                          const void *gamma, void *out, void *residual_out,
+                                          int M, float eps, const skinny_launch_opts *opts,
+                                          void *stream);
 
 /*
  * decode_gemm_bf16_reduce_rmsnorm -- a row-parallel drafter linear whose output
@@ -200,12 +237,20 @@ SKINNY_API int reduce_residual_rmsnorm(const void *partials, int TP, const void 
  *   K % 8 == 0; eps > 0, finite. Needs at least 56 SMs. Uses the decode GEMM's
  *   per-device scratch, like decode_gemm_bf16 (same rules on streams).
  *   Errors: SKINNY_ERR_NULL, _SHAPE, _ALIGN, _ALIAS, _ARG, _DEVICE, _CAPTURE,
- *   _ALLOC, _LAUNCH.
+ *   _ALLOC, _LAUNCH, _TIMEOUT (as decode_gemm_bf16).
  */
 SKINNY_API int decode_gemm_bf16_reduce_rmsnorm(const void *x, const void *W, void *partials,
                                                int TP, const void *residual, const void *gamma,
                                                void *out, void *residual_out, int M, int K,
                                                float eps, void *stream);
+
+/* decode_gemm_bf16_reduce_rmsnorm with per-call launch settings (as
+ * decode_gemm_bf16_ex). */
+SKINNY_API int decode_gemm_bf16_reduce_rmsnorm_ex(const void *x, const void *W, void *partials,
+                                                  int TP, const void *residual,
+                                                  const void *gamma, void *out,
+                                                  void *residual_out, int M, int K, float eps,
+                                                  const skinny_launch_opts *opts, void *stream);
 
 /* Largest TP and row count of gather_shards_bf16. */
 #define SKINNY_GATHER_MAX_TP 64
@@ -213,8 +258,8 @@ SKINNY_API int decode_gemm_bf16_reduce_rmsnorm(const void *x, const void *W, voi
 
 /*
  * gather_shards_bf16 -- every rank's shard into the gathered rows, locally
- *   ("drafter/comm": Gather -- "Every rank's [M, S] ... shard -> the [cap, TP * S]
- *    mailbox rows", "rank r's at columns r S .."; gather_context builds
+ *   ("drafter/comm": Gather places each rank's [M, S] shard side by side in rows
+ *    of TP * S columns, rank r starting at column r * S; gather_context builds
  *    [M, 7168] from [M, 7168 / TP], gather_logits [M, V] from [M, V / TP]. Here
  *    the TP shards are local slots, as in the pages' one-GPU stand-in of
  *    "cutedsl/common/twoshot".)
@@ -238,9 +283,10 @@ SKINNY_API const char *skinny_status_string(int status);
  * skinny_device_error -- read and clear the error word of `device`
  *   Synchronises the device, then returns SKINNY_OK if no kernel of this library
  *   recorded a problem since the last read, else SKINNY_ERR_TIMEOUT, and writes
- *   the raw word (a bit set per waiting role that gave up) to *word if word is
- *   not NULL. Clearing also re-arms the decode GEMM's scratch flags, so the
- *   next call starts clean. Host pointer: word.
+ *   the raw word (a bit set per waiting role that gave up; 64 if only the
+ *   host-mapped word was set) to *word if word is not NULL. Clearing also
+ *   re-arms the decode GEMM's scratch flags, so the next call starts clean and
+ *   calls stop returning SKINNY_ERR_TIMEOUT. Host pointer: word.
  */
 SKINNY_API int skinny_device_error(int device, int *word);
 

@@ -34,6 +34,20 @@ class SkinnyError(RuntimeError):
         super().__init__(f"{where}: {STATUS.get(status, status)} ({status_string(status)})")
 
 
+class LaunchOpts(ctypes.Structure):
+    """skinny_launch_opts: per-call settings, -1 = the process-wide one."""
+    _fields_ = [("pdl", ctypes.c_int), ("l2_prefetch", ctypes.c_int)]
+
+
+def _opts(pdl, l2_prefetch):
+    """A LaunchOpts for the given keywords, or None if both are None (the call
+    then goes to the plain entry point and the process-wide settings)."""
+    if pdl is None and l2_prefetch is None:
+        return None
+    return LaunchOpts(-1 if pdl is None else int(bool(pdl)),
+                      -1 if l2_prefetch is None else int(l2_prefetch))
+
+
 class GemmPlan(ctypes.Structure):
     _fields_ = [("tiles", ctypes.c_int), ("kblocks", ctypes.c_int),
                 ("blocks", ctypes.c_longlong), ("ctas", ctypes.c_int),
@@ -54,15 +68,23 @@ def load_library(path: str = LIBRARY):
                       "`python -m skinny_bf16_gemm_gb300.build`")
     lib = ctypes.CDLL(path)
     vp, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    op = ctypes.POINTER(LaunchOpts)
     lib.decode_gemm_bf16.argtypes = [vp, vp, vp, i32, i32, i32, vp]
     lib.decode_gemm_bf16.restype = i32
+    lib.decode_gemm_bf16_ex.argtypes = [vp, vp, vp, i32, i32, i32, op, vp]
+    lib.decode_gemm_bf16_ex.restype = i32
     lib.reduce_residual_rmsnorm.argtypes = [vp, i32, vp, vp, vp, vp, i32, f32, vp]
     lib.reduce_residual_rmsnorm.restype = i32
+    lib.reduce_residual_rmsnorm_ex.argtypes = [vp, i32, vp, vp, vp, vp, i32, f32, op, vp]
+    lib.reduce_residual_rmsnorm_ex.restype = i32
     lib.decode_gemm_bf16_logits.argtypes = [vp, vp, vp, i32, i32, i32, i32, f32, f32, vp]
     lib.decode_gemm_bf16_logits.restype = i32
     lib.decode_gemm_bf16_reduce_rmsnorm.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, i32, i32,
                                                     f32, vp]
     lib.decode_gemm_bf16_reduce_rmsnorm.restype = i32
+    lib.decode_gemm_bf16_reduce_rmsnorm_ex.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, i32, i32,
+                                                       f32, op, vp]
+    lib.decode_gemm_bf16_reduce_rmsnorm_ex.restype = i32
     lib.gather_shards_bf16.argtypes = [vp, i32, i32, i32, vp, vp]
     lib.gather_shards_bf16.restype = i32
     lib.skinny_status_string.argtypes = [i32]
@@ -112,10 +134,12 @@ def _bf16_cuda(t, name, shape=None):
         raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
 
 
-def decode_gemm_bf16(x, W, out, stream=None):
+def decode_gemm_bf16(x, W, out, stream=None, pdl=None, l2_prefetch=None):
     """out[M, N] = x[M, K] @ W[N, K]^T on the current (or given) stream.
 
-    x, W, out: contiguous CUDA bfloat16 tensors. Returns ``out``.
+    x, W, out: contiguous CUDA bfloat16 tensors. Returns ``out``. pdl and
+    l2_prefetch, when given, are this call's launch settings (decode_gemm_bf16_ex)
+    instead of the process-wide ones.
     """
     _bf16_cuda(x, "x")
     _bf16_cuda(W, "W")
@@ -124,8 +148,14 @@ def decode_gemm_bf16(x, W, out, stream=None):
     M, K = x.shape
     N = W.shape[0]
     _bf16_cuda(out, "out", (M, N))
-    st = load_library().decode_gemm_bf16(x.data_ptr(), W.data_ptr(), out.data_ptr(), M, N, K,
-                                         _stream_handle(stream))
+    o = _opts(pdl, l2_prefetch)
+    lib = load_library()
+    if o is None:
+        st = lib.decode_gemm_bf16(x.data_ptr(), W.data_ptr(), out.data_ptr(), M, N, K,
+                                  _stream_handle(stream))
+    else:
+        st = lib.decode_gemm_bf16_ex(x.data_ptr(), W.data_ptr(), out.data_ptr(), M, N, K,
+                                     ctypes.byref(o), _stream_handle(stream))
     _check(st, "decode_gemm_bf16")
     return out
 
@@ -149,11 +179,12 @@ def decode_gemm_bf16_logits(x, W, out, soft_cap=0.0, scale=1.0, stream=None):
 
 
 def reduce_residual_rmsnorm(partials, residual, gamma, out, residual_out, eps=1e-6,
-                            stream=None):
+                            stream=None, pdl=None):
     """(out, residual_out) of the rank-order reduce + residual + RMSNorm.
 
     partials [TP, M, 7168], residual [M, 7168] or None, gamma [7168],
-    out and residual_out [M, 7168]; all contiguous CUDA bfloat16.
+    out and residual_out [M, 7168]; all contiguous CUDA bfloat16. pdl, when
+    given, is this call's setting (reduce_residual_rmsnorm_ex).
     """
     _bf16_cuda(partials, "partials")
     if partials.dim() != 3 or partials.shape[2] != HIDDEN:
@@ -164,23 +195,27 @@ def reduce_residual_rmsnorm(partials, residual, gamma, out, residual_out, eps=1e
     _bf16_cuda(gamma, "gamma", (HIDDEN,))
     _bf16_cuda(out, "out", (M, HIDDEN))
     _bf16_cuda(residual_out, "residual_out", (M, HIDDEN))
-    st = load_library().reduce_residual_rmsnorm(
-        partials.data_ptr(), TP, None if residual is None else residual.data_ptr(),
-        gamma.data_ptr(), out.data_ptr(), residual_out.data_ptr(), M, float(eps),
-        _stream_handle(stream))
+    args = (partials.data_ptr(), TP, None if residual is None else residual.data_ptr(),
+            gamma.data_ptr(), out.data_ptr(), residual_out.data_ptr(), M, float(eps))
+    o = _opts(pdl, None)
+    if o is None:
+        st = load_library().reduce_residual_rmsnorm(*args, _stream_handle(stream))
+    else:
+        st = load_library().reduce_residual_rmsnorm_ex(*args, ctypes.byref(o),
+                                                       _stream_handle(stream))
     _check(st, "reduce_residual_rmsnorm")
     return out, residual_out
 
 
 def decode_gemm_bf16_reduce_rmsnorm(x, W, partials, residual, gamma, out, residual_out,
-                                    eps=1e-6, stream=None):
+                                    eps=1e-6, stream=None, pdl=None, l2_prefetch=None):
     """The row-parallel linear with the reduce + residual + RMSNorm after it.
 
     x [M, K], W [7168, K]; partials [TP, M, 7168] (slot 0 receives x @ W^T,
     slots 1.. are read); residual [M, 7168] or None; gamma [7168]; out and
     residual_out [M, 7168]; all contiguous CUDA bfloat16. Returns
     (out, residual_out), bit for bit those of decode_gemm_bf16 followed by
-    reduce_residual_rmsnorm.
+    reduce_residual_rmsnorm. pdl and l2_prefetch as for decode_gemm_bf16.
     """
     _bf16_cuda(x, "x")
     _bf16_cuda(W, "W")
@@ -196,10 +231,15 @@ def decode_gemm_bf16_reduce_rmsnorm(x, W, partials, residual, gamma, out, residu
     _bf16_cuda(gamma, "gamma", (HIDDEN,))
     _bf16_cuda(out, "out", (M, HIDDEN))
     _bf16_cuda(residual_out, "residual_out", (M, HIDDEN))
-    st = load_library().decode_gemm_bf16_reduce_rmsnorm(
-        x.data_ptr(), W.data_ptr(), partials.data_ptr(), TP,
-        None if residual is None else residual.data_ptr(), gamma.data_ptr(), out.data_ptr(),
-        residual_out.data_ptr(), M, K, float(eps), _stream_handle(stream))
+    args = (x.data_ptr(), W.data_ptr(), partials.data_ptr(), TP,
+            None if residual is None else residual.data_ptr(), gamma.data_ptr(), out.data_ptr(),
+            residual_out.data_ptr(), M, K, float(eps))
+    o = _opts(pdl, l2_prefetch)
+    if o is None:
+        st = load_library().decode_gemm_bf16_reduce_rmsnorm(*args, _stream_handle(stream))
+    else:
+        st = load_library().decode_gemm_bf16_reduce_rmsnorm_ex(*args, ctypes.byref(o),
+                                                               _stream_handle(stream))
     _check(st, "decode_gemm_bf16_reduce_rmsnorm")
     return out, residual_out
 

@@ -14,24 +14,26 @@ second GEMM and the reduce + residual + RMSNorm are one call,
 decode_gemm_bf16_reduce_rmsnorm (bit-identical results, two kernels instead of a
 split-K fix-up inside the GEMM plus a reduce). Every step of the chain runs in
 the library's kernels; this class only owns the device buffers and orders the
-calls on one stream (optionally as one CUDA graph). While it enqueues a step it
-sets the decode GEMM's L2 lead (set_l2_prefetch) to l2_prefetch, 0 by default:
+calls on one stream (optionally as one CUDA graph). Every call carries the
+chain's own launch settings (the library's _ex entry points), so the chain never
+changes the process-wide ones other code sees: programmatic dependent launch
+(pdl, on by default) and the decode GEMM's L2 lead (l2_prefetch, 0 by default:
 measured on GB300, each GEMM of the chain runs behind or ahead of a short
 kernel, and weight prefetches issued before the PDL wait only slow the previous
-GEMM's last CTAs there (chain step 0.7-0.8 % faster than with the default 6).
+GEMM's last CTAs there; chain step 0.7-0.8 % faster than with the default 6).
 """
 import torch
 
-from . import (decode_gemm_bf16, decode_gemm_bf16_reduce_rmsnorm, reduce_residual_rmsnorm,
-               set_l2_prefetch, set_pdl)
+from . import decode_gemm_bf16, decode_gemm_bf16_reduce_rmsnorm, reduce_residual_rmsnorm
 
 
 class LayerChain:
     def __init__(self, W1, W2, peers, gamma, M, eps=1e-6, device="cuda", fused=False,
-                 l2_prefetch=0):
+                 l2_prefetch=0, pdl=True):
         self.layers = len(W1)
         self.fused = fused
         self.l2_prefetch = l2_prefetch
+        self.pdl = bool(pdl)
         self.W1, self.W2, self.gamma = W1, W2, gamma
         self.M, self.eps = M, eps
         self.F, self.H = W1[0].shape
@@ -59,53 +61,45 @@ class LayerChain:
 
         on_launch(kind, layer, phase) is called with phase 'before' / 'after'
         around every launch (used to bracket kernels with timing events)."""
-        prev = set_l2_prefetch(self.l2_prefetch)
-        try:
-            return self._enqueue(stream, on_launch)
-        finally:
-            set_l2_prefetch(prev)
-
-    def _enqueue(self, stream, on_launch):
+        gemm_opts = dict(pdl=self.pdl, l2_prefetch=self.l2_prefetch)
         x, res = self.x, self.res_in
         for l in range(self.layers):
             if on_launch:
                 on_launch("gemm", l, "before")
-            decode_gemm_bf16(x, self.W1[l], self.h1, stream)
+            decode_gemm_bf16(x, self.W1[l], self.h1, stream, **gemm_opts)
             if on_launch:
                 on_launch("gemm", l, "after")
                 on_launch("gemm", l, "before")
             out, res_out = self.outs[l % 2], self.res[l % 2]
             if self.fused:
                 decode_gemm_bf16_reduce_rmsnorm(self.h1, self.W2[l], self.partials[l], res,
-                                                self.gamma[l], out, res_out, self.eps, stream)
+                                                self.gamma[l], out, res_out, self.eps, stream,
+                                                **gemm_opts)
                 if on_launch:
                     on_launch("gemm", l, "after")
             else:
-                decode_gemm_bf16(self.h1, self.W2[l], self.partials[l][0], stream)
+                decode_gemm_bf16(self.h1, self.W2[l], self.partials[l][0], stream, **gemm_opts)
                 if on_launch:
                     on_launch("gemm", l, "after")
                     on_launch("reduce", l, "before")
                 reduce_residual_rmsnorm(self.partials[l], res, self.gamma[l], out, res_out,
-                                        self.eps, stream)
+                                        self.eps, stream, pdl=self.pdl)
                 if on_launch:
                     on_launch("reduce", l, "after")
             x, res = out, res_out
         return x, res
 
-    def capture(self, pdl=False):
-        """Capture one step as a CUDA graph (after at least one eager step)."""
-        prev = set_pdl(pdl)
-        try:
-            s = torch.cuda.Stream()
-            s.wait_stream(torch.cuda.current_stream())
-            with torch.cuda.stream(s):
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g, stream=s):
-                    self.graph_out = self.run()
-            torch.cuda.current_stream().wait_stream(s)
-            self.graph = g
-        finally:
-            set_pdl(prev)
+    def capture(self):
+        """Capture one step as a CUDA graph (after at least one eager step), with
+        the chain's launch settings."""
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                self.graph_out = self.run()
+        torch.cuda.current_stream().wait_stream(s)
+        self.graph = g
         return self.graph_out
 
     def replay(self):

@@ -29,6 +29,12 @@ struct DeviceState {
     unsigned *flags = nullptr;
     int *err = nullptr;
     size_t flag_bytes = 0;
+    // A host-mapped word the decode GEMM sets when one of its waits runs out:
+    // the host reads it without synchronising, so the next call can refuse to
+    // run on scratch a kernel left half used (host_err) -- and the kernel's
+    // address of it (host_err_dev).
+    int *host_err = nullptr;
+    int *host_err_dev = nullptr;
 };
 
 std::mutex g_mutex;
@@ -99,6 +105,21 @@ int ensure_scratch(int dev, cudaStream_t stream, DeviceState **out) {
             cudaFree(p);
             return SKINNY_ERR_ALLOC;
         }
+        void *h = nullptr, *hd = nullptr;
+        if (cudaHostAlloc(&h, 256, cudaHostAllocMapped | cudaHostAllocPortable) != cudaSuccess) {
+            cudaGetLastError();
+            cudaFree(p);
+            return SKINNY_ERR_ALLOC;
+        }
+        if (cudaHostGetDevicePointer(&hd, h, 0) != cudaSuccess) {
+            cudaGetLastError();
+            cudaFreeHost(h);
+            cudaFree(p);
+            return SKINNY_ERR_ALLOC;
+        }
+        std::memset(h, 0, 256);
+        d->host_err = static_cast<int *>(h);
+        d->host_err_dev = static_cast<int *>(hd);
         d->scratch = p;
         d->partials = static_cast<float *>(p);
         d->flags = reinterpret_cast<unsigned *>(static_cast<char *>(p) + partial_bytes);
@@ -166,9 +187,41 @@ int gemm_shape_ok(int M, int N, int K) {
 
 int mma_n_for(int M) { return M <= 16 ? 16 : (M <= 32 ? 32 : 64); }
 
+// SKINNY_ERR_TIMEOUT while a decode GEMM on this device has recorded a wait that
+// ran out and skinny_device_error() has not cleared it: the split-K scratch
+// may hold flags that kernel never consumed, so nothing that uses it runs.
+int pending_timeout(const DeviceState *d) {
+    if (d->host_err != nullptr && *reinterpret_cast<volatile const int *>(d->host_err) != 0)
+        return SKINNY_ERR_TIMEOUT;
+    return SKINNY_OK;
+}
+
+// The launch settings of one call: the caller's options where given, else the
+// process-wide settings (skinny_set_pdl, skinny_set_l2_prefetch).
+struct LaunchSettings {
+    bool pdl;
+    int l2_lead;
+};
+
+int resolve_settings(const skinny_launch_opts *opts, LaunchSettings *out) {
+    if (opts != nullptr) {
+        if (opts->pdl < SKINNY_OPT_DEFAULT || opts->pdl > 1) return SKINNY_ERR_ARG;
+        if (opts->l2_prefetch < SKINNY_OPT_DEFAULT || opts->l2_prefetch > kL2LeadMax)
+            return SKINNY_ERR_ARG;
+    }
+    std::lock_guard<std::mutex> lock(g_mutex);
+    out->pdl = g_pdl;
+    out->l2_lead = g_l2_lead;
+    if (opts != nullptr) {
+        if (opts->pdl != SKINNY_OPT_DEFAULT) out->pdl = opts->pdl != 0;
+        if (opts->l2_prefetch != SKINNY_OPT_DEFAULT) out->l2_lead = opts->l2_prefetch;
+    }
+    return SKINNY_OK;
+}
+
 int gemm_launch(const void *x, const void *W, void *out, int M, int N, int K, void *stream,
-                int selftest, unsigned long long limit_ns, int logits = 0, float soft_cap = 0.0f,
-                float scale = 1.0f) {
+                const skinny_launch_opts *opts, int selftest, unsigned long long limit_ns,
+                int logits = 0, float soft_cap = 0.0f, float scale = 1.0f) {
     if (!x || !W || !out) return SKINNY_ERR_NULL;
     int st = gemm_shape_ok(M, N, K);
     if (st) return st;
@@ -176,6 +229,8 @@ int gemm_launch(const void *x, const void *W, void *out, int M, int N, int K, vo
     const size_t xb = static_cast<size_t>(M) * K * 2, wb = static_cast<size_t>(N) * K * 2,
                  ob = static_cast<size_t>(M) * N * 2;
     if (overlaps(out, ob, x, xb) || overlaps(out, ob, W, wb)) return SKINNY_ERR_ALIAS;
+    LaunchSettings ls;
+    if ((st = resolve_settings(opts, &ls))) return st;
     int dev;
     if ((st = current_device(&dev))) return st;
     if ((st = check_device_pointer(x, dev)) || (st = check_device_pointer(W, dev)) ||
@@ -184,6 +239,7 @@ int gemm_launch(const void *x, const void *W, void *out, int M, int N, int K, vo
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     DeviceState *d = nullptr;
     if ((st = ensure_scratch(dev, s, &d))) return st;
+    if ((st = pending_timeout(d))) return st;
     EncodeTiledFn enc;
     if ((st = encoder(&enc))) return st;
     const int mma_n = mma_n_for(M);
@@ -200,17 +256,14 @@ int gemm_launch(const void *x, const void *W, void *out, int M, int N, int K, vo
     a.slot_floats = kSlotFloats;
     a.flags = d->flags;
     a.err = d->err;
+    a.host_err = d->host_err_dev;
     a.wait_limit_ns = limit_ns;
     a.selftest = selftest;
     a.logits = logits;
     a.soft_cap = soft_cap;
     a.scale = scale;
-    bool pdl;
-    {
-        std::lock_guard<std::mutex> lock(g_mutex);
-        pdl = g_pdl;
-        a.l2_lead = g_l2_lead;
-    }
+    const bool pdl = ls.pdl;
+    a.l2_lead = ls.l2_lead;
     // Split tiles of 64-row accumulators, every CTA within at most two tiles (two
     // scratch slots), plain output: the GEMM only publishes its partials and a
     // small kernel finishes them (same order, same bits). A finisher CTA would
@@ -341,7 +394,12 @@ using namespace skinny;
 extern "C" {
 
 int decode_gemm_bf16(const void *x, const void *W, void *out, int M, int N, int K, void *stream) {
-    return gemm_launch(x, W, out, M, N, K, stream, 0, kWaitLimitNs);
+    return gemm_launch(x, W, out, M, N, K, stream, nullptr, 0, kWaitLimitNs);
+}
+
+int decode_gemm_bf16_ex(const void *x, const void *W, void *out, int M, int N, int K,
+                        const skinny_launch_opts *opts, void *stream) {
+    return gemm_launch(x, W, out, M, N, K, stream, opts, 0, kWaitLimitNs);
 }
 
 int decode_gemm_bf16_noalloc(const void *x, const void *W, void *out, int M, int N, int K,
@@ -349,9 +407,10 @@ int decode_gemm_bf16_noalloc(const void *x, const void *W, void *out, int M, int
     return gemm_launch_static(x, W, out, M, N, K, stream);
 }
 
-int decode_gemm_bf16_reduce_rmsnorm(const void *x, const void *W, void *partials, int TP,
-                                    const void *residual, const void *gamma, void *out,
-                                    void *residual_out, int M, int K, float eps, void *stream) {
+int decode_gemm_bf16_reduce_rmsnorm_ex(const void *x, const void *W, void *partials, int TP,
+                                       const void *residual, const void *gamma, void *out,
+                                       void *residual_out, int M, int K, float eps,
+                                       const skinny_launch_opts *opts, void *stream) {
     constexpr int N = SKINNY_HIDDEN;
     if (!x || !W || !partials || !gamma || !out || !residual_out) return SKINNY_ERR_NULL;
     if (M < 1 || M > SKINNY_REDUCE_MAX_M || TP < 1 || TP > SKINNY_REDUCE_MAX_TP) return SKINNY_ERR_SHAPE;
@@ -374,6 +433,8 @@ int decode_gemm_bf16_reduce_rmsnorm(const void *x, const void *W, void *partials
         (residual && (overlaps(out, row, residual, row) || overlaps(partials, pb, residual, row) ||
                       (residual != residual_out && overlaps(residual_out, row, residual, row)))))
         return SKINNY_ERR_ALIAS;
+    LaunchSettings ls;
+    if ((st = resolve_settings(opts, &ls))) return st;
     int dev;
     if ((st = current_device(&dev))) return st;
     if ((st = check_device_pointer(x, dev)) || (st = check_device_pointer(W, dev)) ||
@@ -384,6 +445,7 @@ int decode_gemm_bf16_reduce_rmsnorm(const void *x, const void *W, void *partials
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     DeviceState *d = nullptr;
     if ((st = ensure_scratch(dev, s, &d))) return st;
+    if ((st = pending_timeout(d))) return st;
     const GemmGeometry g = make_geometry(M, N, K, choose_ctas(N, d->sms));
     // The scratch holds two partial slots per CTA: every CTA's range must touch
     // at most two tiles, which at least one CTA per tile guarantees.
@@ -394,13 +456,8 @@ int decode_gemm_bf16_reduce_rmsnorm(const void *x, const void *W, void *partials
     alignas(64) CUtensorMap w_map, x_map;
     if ((st = encode_2d(enc, &w_map, W, N, K, kBlockN))) return st;
     if ((st = encode_2d(enc, &x_map, x, M, K, mma_n))) return st;
-    bool pdl;
-    int l2_lead;
-    {
-        std::lock_guard<std::mutex> lock(g_mutex);
-        pdl = g_pdl;
-        l2_lead = g_l2_lead;
-    }
+    const bool pdl = ls.pdl;
+    const int l2_lead = ls.l2_lead;
     GemmArgs a = {};
     a.M = M;
     a.N = N;
@@ -410,6 +467,7 @@ int decode_gemm_bf16_reduce_rmsnorm(const void *x, const void *W, void *partials
     a.slot_floats = kSlotFloats;
     a.flags = d->flags;
     a.err = d->err;
+    a.host_err = d->host_err_dev;
     a.wait_limit_ns = kWaitLimitNs;
     a.scale = 1.0f;
     a.publish_only = 1;
@@ -437,25 +495,32 @@ int decode_gemm_bf16_reduce_rmsnorm(const void *x, const void *W, void *partials
     return SKINNY_OK;
 }
 
+int decode_gemm_bf16_reduce_rmsnorm(const void *x, const void *W, void *partials, int TP,
+                                    const void *residual, const void *gamma, void *out,
+                                    void *residual_out, int M, int K, float eps, void *stream) {
+    return decode_gemm_bf16_reduce_rmsnorm_ex(x, W, partials, TP, residual, gamma, out,
+                                              residual_out, M, K, eps, nullptr, stream);
+}
+
 int decode_gemm_bf16_logits(const void *x, const void *W, void *out, int M, int N, int K,
                             int n_out, float soft_cap, float scale, void *stream) {
     if (n_out < 1 || n_out > N) return SKINNY_ERR_SHAPE;
     if (!std::isfinite(soft_cap) || !std::isfinite(scale)) return SKINNY_ERR_ARG;
     // Only the first n_out weight rows are read: the same GEMM with N = n_out.
-    return gemm_launch(x, W, out, M, n_out, K, stream, 0, kWaitLimitNs, 1,
+    return gemm_launch(x, W, out, M, n_out, K, stream, nullptr, 0, kWaitLimitNs, 1,
                        soft_cap > 0.0f ? soft_cap : 0.0f, scale);
 }
 
 int skinny_watchdog_selftest(const void *x, const void *W, void *out, int M, int N, int K,
                              long long timeout_ns, void *stream) {
     if (timeout_ns < 1000 || timeout_ns > 2000000000LL) return SKINNY_ERR_ARG;
-    return gemm_launch(x, W, out, M, N, K, stream, 1,
+    return gemm_launch(x, W, out, M, N, K, stream, nullptr, 1,
                        static_cast<unsigned long long>(timeout_ns));
 }
 
-int reduce_residual_rmsnorm(const void *partials, int TP, const void *residual,
-                            const void *gamma, void *out, void *residual_out, int M, float eps,
-                            void *stream) {
+int reduce_residual_rmsnorm_ex(const void *partials, int TP, const void *residual,
+                               const void *gamma, void *out, void *residual_out, int M, float eps,
+                               const skinny_launch_opts *opts, void *stream) {
     if (!partials || !gamma || !out || !residual_out) return SKINNY_ERR_NULL;
     if (TP < 1 || TP > SKINNY_REDUCE_MAX_TP || M < 1 || M > SKINNY_REDUCE_MAX_M)
         return SKINNY_ERR_SHAPE;
@@ -473,6 +538,8 @@ int reduce_residual_rmsnorm(const void *partials, int TP, const void *residual,
     if (residual && residual != residual_out && overlaps(residual_out, row, residual, row))
         return SKINNY_ERR_ALIAS;
     int dev, st;
+    LaunchSettings ls;
+    if ((st = resolve_settings(opts, &ls))) return st;
     if ((st = current_device(&dev))) return st;
     DeviceState *d = nullptr;
     if ((st = device_state(dev, &d))) return st;
@@ -480,19 +547,21 @@ int reduce_residual_rmsnorm(const void *partials, int TP, const void *residual,
         (st = check_device_pointer(out, dev)) || (st = check_device_pointer(residual_out, dev)) ||
         (residual && (st = check_device_pointer(residual, dev))))
         return st;
-    bool pdl;
-    {
-        std::lock_guard<std::mutex> lock(g_mutex);
-        pdl = g_pdl;
-    }
     cudaError_t e = launch_reduce_rmsnorm(partials, TP, residual, gamma, out, residual_out, M, eps,
                                           reduce_ctas_per_row(M, TP, residual != nullptr),
-                                          static_cast<cudaStream_t>(stream), pdl);
+                                          static_cast<cudaStream_t>(stream), ls.pdl);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return SKINNY_ERR_LAUNCH;
     }
     return SKINNY_OK;
+}
+
+int reduce_residual_rmsnorm(const void *partials, int TP, const void *residual,
+                            const void *gamma, void *out, void *residual_out, int M, float eps,
+                            void *stream) {
+    return reduce_residual_rmsnorm_ex(partials, TP, residual, gamma, out, residual_out, M, eps,
+                                      nullptr, stream);
 }
 
 int gather_shards_bf16(const void *shards, int TP, int M, int S, void *out, void *stream) {
@@ -559,12 +628,16 @@ int skinny_device_error(int device, int *word) {
             if (cudaMemcpy(&value, d.err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) {
                 cudaGetLastError();
                 st = SKINNY_ERR_DEVICE;
-            } else if (value != 0) {
-                // A kernel gave up part-way: clear the word and the partial flags.
+            } else if (value != 0 || *reinterpret_cast<volatile int *>(d.host_err) != 0) {
+                // A kernel gave up part-way: clear the words and the partial flags,
+                // which lets later calls run again.
                 if (cudaMemset(d.err, 0, sizeof(int)) != cudaSuccess ||
                     cudaMemset(d.flags, 0, d.flag_bytes) != cudaSuccess) {
                     cudaGetLastError();
                     st = SKINNY_ERR_DEVICE;
+                } else {
+                    if (value == 0) value = kErrUnknown;
+                    *reinterpret_cast<volatile int *>(d.host_err) = 0;
                 }
             }
         }
@@ -623,14 +696,15 @@ int skinny_gemm_cta_pieces(int M, int N, int K, int num_sms, int cta, int *tile,
     if (!tile || !kb0 || !kb1 || !slot || num_sms < 1 || gemm_shape_ok(M, N, K)) return -1;
     const GemmGeometry g = make_geometry(M, N, K, choose_ctas(N, num_sms));
     if (cta < 0 || cta >= g.ctas) return -1;
-    const int n = cta_piece_count(g, cta);
+    const int r = range_of_block(g, cta);
+    const int n = cta_piece_count(g, r);
     for (int q = 0; q < n && q < max_pieces; ++q) {
-        const Piece p = cta_piece(g, cta, q);
+        const Piece p = cta_piece(g, r, q);
         tile[q] = p.tile;
         kb0[q] = p.kb0;
         kb1[q] = p.kb1;
         const bool whole = p.kb0 == 0 && p.kb1 == g.kblocks;
-        slot[q] = whole ? -1 : partial_slot(g, cta, p.tile);
+        slot[q] = whole ? -1 : partial_slot(g, r, p.tile);
     }
     return n;
 }

@@ -18,7 +18,8 @@
 // by several CTAs is finished by the CTA holding its first K blocks (for which it
 // is the last piece): the others publish their FP32 partials behind a release
 // flag, and the finisher adds them in K order, so the bits do not depend on
-// timing.
+// timing. Ranges go to CTAs in reverse block order, so a finisher waits only on
+// CTAs with lower block indices, which the GPU dispatched before it.
 // Ring depth (plan.cuh use_shallow_ring): the deep ring, one CTA per SM, for
 // long streams; the shallow ring for short ones under programmatic dependent
 // launch, so that the next kernel's CTA shares the SM. Before waiting on the
@@ -94,8 +95,20 @@ __device__ __forceinline__ int bounded_wait(uint32_t bar, uint32_t parity,
     }
 }
 
-__device__ __forceinline__ void raise_error(int *err, volatile uint32_t *abort_flag, int bit) {
-    atomicOr(err, bit);
+// Record a problem: the bit in the device error word, and a nonzero word in the
+// caller's host-mapped memory when there is one (the host reads it without
+// synchronising, so the library's next call can report it).
+__device__ __forceinline__ void record_error(const GemmArgs &a, int bit) {
+    atomicOr(a.err, bit);
+    if (a.host_err != nullptr) {
+        *reinterpret_cast<volatile int *>(a.host_err) = 1;
+        __threadfence_system();
+    }
+}
+
+__device__ __forceinline__ void raise_error(const GemmArgs &a, volatile uint32_t *abort_flag,
+                                            int bit) {
+    record_error(a, bit);
     *abort_flag = 1u;
 }
 
@@ -147,8 +160,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
-    const int cta = blockIdx.x;
     const GemmGeometry g = make_geometry(args.M, args.N, args.K, gridDim.x);
+    // This CTA's range of weight blocks (plan.cuh: reverse block order, so the
+    // split-K finisher below waits only on CTAs with lower block indices).
+    const int cta = range_of_block(g, static_cast<int>(blockIdx.x));
     const uint64_t limit = args.wait_limit_ns;
 
     if (threadIdx.x == 0) {
@@ -229,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (long long j = npre; j < total; ++j) {
                 const int r = bounded_wait(bar_empty + 8 * s, ph ^ 1u, abort_flag, limit);
                 if (r != kWaitDone) {
-                    if (r == kWaitTimeout) raise_error(args.err, abort_flag, kErrProducerWait);
+                    if (r == kWaitTimeout) raise_error(args, abort_flag, kErrProducerWait);
                     break;
                 }
                 const long long blk = b0 + j;
@@ -259,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (args.selftest) {
                 // Wait on a barrier nothing ever completes: exercises the bounded wait.
                 const int r = bounded_wait(bar_never, 0, abort_flag, limit);
-                if (r == kWaitTimeout) raise_error(args.err, abort_flag, kErrSelftest);
+                if (r == kWaitTimeout) raise_error(args, abort_flag, kErrSelftest);
                 ok = false;
             }
             for (int q = 0; ok && q < pieces; ++q) {
@@ -268,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t aph = (q >> 1) & 1;
                 int r = bounded_wait(bar_acc_empty + 8 * b, aph ^ 1u, abort_flag, limit);
                 if (r != kWaitDone) {
-                    if (r == kWaitTimeout) raise_error(args.err, abort_flag, kErrMmaAccWait);
+                    if (r == kWaitTimeout) raise_error(args, abort_flag, kErrMmaAccWait);
                     ok = false;
                     break;
                 }
@@ -277,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kb = p.kb0; kb < p.kb1; ++kb) {
                     r = bounded_wait(bar_full + 8 * s, ph, abort_flag, limit);
                     if (r != kWaitDone) {
-                        if (r == kWaitTimeout) raise_error(args.err, abort_flag, kErrMmaFullWait);
+                        if (r == kWaitTimeout) raise_error(args, abort_flag, kErrMmaFullWait);
                         ok = false;
                         break;
                     }
@@ -357,10 +372,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                        slot_bytes, bar_fix);
                     }
                 }
-                if (r == kWaitTimeout) raise_error(args.err, abort_flag, kErrEpilogueWait);
+                if (r == kWaitTimeout) raise_error(args, abort_flag, kErrEpilogueWait);
                 if (epilogue_any(r != kWaitDone)) return false;
                 r = bounded_wait(bar_fix, fix_phase, abort_flag, limit);
-                if (r == kWaitTimeout) raise_error(args.err, abort_flag, kErrEpilogueWait);
+                if (r == kWaitTimeout) raise_error(args, abort_flag, kErrEpilogueWait);
                 if (epilogue_any(r != kWaitDone)) return false;
                 fix_pending = false;
                 fix_phase ^= 1u;
@@ -397,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int b = q & 1;
             const uint32_t aph = (q >> 1) & 1;
             const int r = bounded_wait(bar_acc_full + 8 * b, aph, abort_flag, limit);
-            if (r == kWaitTimeout) raise_error(args.err, abort_flag, kErrEpilogueWait);
+            if (r == kWaitTimeout) raise_error(args, abort_flag, kErrEpilogueWait);
             if (epilogue_any(r != kWaitDone)) break;
             ptx::tc_fence_after_sync();
             float acc[MP];
@@ -453,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t t0 = ptx::global_timer_ns();
             while (!ptx::mbar_try_wait(bar_fix, fix_phase)) {
                 if (ptx::global_timer_ns() - t0 > kDrainLimitNs) {
-                    atomicOr(args.err, kErrDrain);
+                    record_error(args, kErrDrain);
                     break;
                 }
             }
@@ -471,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint64_t t0 = ptx::global_timer_ns();
                 while (!ptx::mbar_try_wait(bar_full + 8 * s, par)) {
                     if (ptx::global_timer_ns() - t0 > kDrainLimitNs) {
-                        atomicOr(args.err, kErrDrain);
+                        record_error(args, kErrDrain);
                         break;
                     }
                 }
@@ -482,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t t0 = ptx::global_timer_ns();
             while (!ptx::mbar_try_wait(bar_drain, 0)) {
                 if (ptx::global_timer_ns() - t0 > kDrainLimitNs) {
-                    atomicOr(args.err, kErrDrain);
+                    record_error(args, kErrDrain);
                     break;
                 }
             }

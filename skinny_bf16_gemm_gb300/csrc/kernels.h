@@ -15,6 +15,7 @@ enum ErrorBits : int {
     kErrEpilogueWait = 8,   // epilogue: an accumulator never completed
     kErrDrain = 16,         // teardown: in-flight copies or MMAs did not finish
     kErrSelftest = 32,      // the watchdog self-test's deliberate wait ran out
+    kErrUnknown = 64,       // the host-mapped word was set but the device word was not
 };
 
 struct GemmArgs {
@@ -24,6 +25,7 @@ struct GemmArgs {
     int slot_floats;        // floats from one partial tile to the next
     unsigned *flags;        // [2 * ctas] "partial published" flags, zero between calls
     int *err;               // device error word
+    int *host_err;          // host-mapped word set to 1 on any error, or nullptr
     unsigned long long wait_limit_ns;
     int selftest;           // 1: the MMA role waits on a barrier nothing completes
     // lm_head epilogue (logits = 1): v = soft_cap > 0 ? soft_cap * tanh(v / soft_cap)

@@ -2,11 +2,20 @@
 //
 // The weight W[N, K] is cut into tiles of 128 rows (one MMA M extent) and each
 // tile's K range into blocks of 64 (one 128-byte swizzle row of BF16). The
-// tiles * kblocks weight blocks, in tile-major order, are dealt to G persistent
-// CTAs as contiguous ranges of (almost) equal length ("stream-K"): every CTA
+// tiles * kblocks weight blocks, in tile-major order, are cut into G contiguous
+// ranges of (almost) equal length ("stream-K"), one per persistent CTA: every CTA
 // streams the same number of weight bytes whatever N and K are, so no SM idles
-// in a partial last wave. A tile whose K range spans several CTAs is finished by
-// the last of them to arrive, which adds the others' FP32 partial sums in K order.
+// in a partial last wave. A tile whose K range spans several ranges is finished
+// by the CTA whose range holds the tile's first K blocks, which adds the others'
+// FP32 partial sums in K order.
+//
+// Ranges are numbered in K order (range r precedes range r + 1) and dealt to
+// CTAs in reverse block order (range r to block G - 1 - r). A tile's finisher
+// holds its lowest range, so it has the highest block index of the tile's
+// contributors, and every CTA it waits for has a lower block index: blocks are
+// dispatched in index order, so those are already running (or done) whatever
+// else occupies the GPU, and the waits never depend on all G CTAs being
+// resident at once.
 #pragma once
 
 #include <cstdint>
@@ -66,23 +75,29 @@ __host__ __device__ inline bool use_shallow_ring(const GemmGeometry &g, bool pdl
            per_cta < (g.M <= 16 ? kShallowRingMaxBytes16 : kShallowRingMaxBytes);
 }
 
-// First weight block of CTA c (c = ctas gives the end of the last range).
+// Range of the CTA with block index b, and the block index of the CTA that
+// streams range r (the map is its own inverse).
+__host__ __device__ inline int range_of_block(const GemmGeometry &g, int b) { return g.ctas - 1 - b; }
+
+// In the functions below c is a range index, not a block index.
+
+// First weight block of range c (c = ctas gives the end of the last range).
 __host__ __device__ inline long long cta_begin(const GemmGeometry &g, int c) {
     return (g.blocks * c) / g.ctas;
 }
 
-// The CTA whose range holds weight block i: the largest c with cta_begin(c) <= i.
+// The range holding weight block i: the largest c with cta_begin(c) <= i.
 __host__ __device__ inline int block_owner(const GemmGeometry &g, long long i) {
     return static_cast<int>(((i + 1) * g.ctas - 1) / g.blocks);
 }
 
-// Scratch slot of CTA c's partial sum for tile t: two per CTA, one for the tile
-// its range starts in and one for the tile it ends in.
+// Scratch slot of range c's partial sum for tile t: two per range, one for the
+// tile it starts in and one for the tile it ends in.
 __host__ __device__ inline int partial_slot(const GemmGeometry &g, int c, int t) {
     return 2 * c + (t == static_cast<int>(cta_begin(g, c) / g.kblocks) ? 0 : 1);
 }
 
-// Piece q of CTA c's range: tile t, blocks [kb0, kb1) of it.
+// Piece q of range c: tile t, blocks [kb0, kb1) of it.
 struct Piece {
     int tile, kb0, kb1;
 };
@@ -104,7 +119,7 @@ __host__ __device__ inline Piece cta_piece(const GemmGeometry &g, int c, int q) 
     return p;
 }
 
-// CTAs contributing to tile t: [first, last].
+// Ranges contributing to tile t, in K order: [first, last].
 __host__ __device__ inline void tile_contributors(const GemmGeometry &g, int t, int &first,
                                                   int &last) {
     long long t0 = static_cast<long long>(t) * g.kblocks;

@@ -284,16 +284,48 @@ def test_work_split_covers_every_block_once(lib, M, N, K, sms):
     assert len(seen) == plan.blocks
     # Balanced: every CTA streams the same number of blocks, give or take one.
     assert max(per_cta) - min(per_cta) <= 1
-    # Contributors of a tile are consecutive CTAs, in K order; the counter index
-    # (first contributor) is distinct for every shared tile.
-    firsts = []
+    # Contributors of a tile are consecutive CTAs; ranges go to CTAs in reverse
+    # block order, so along K the block index falls. The finisher (the CTA holding
+    # the tile's first K blocks) is distinct for every shared tile.
+    finishers = []
     for t, cs in contributors.items():
+        cs = sorted(cs)
         assert cs == list(range(cs[0], cs[0] + len(cs)))
         order = [seen[(t, kb)] for kb in range(plan.kblocks)]
-        assert order == sorted(order)
+        assert order == sorted(order, reverse=True)
         if len(cs) > 1:
-            firsts.append(cs[0])
-    assert len(firsts) == len(set(firsts)) == plan.split_tiles
+            finishers.append(seen[(t, 0)])
+    assert len(finishers) == len(set(finishers)) == plan.split_tiles
+
+
+@pytest.mark.parametrize("M,N,K,sms", SHAPES)
+def test_split_k_waits_point_to_lower_block_indices(lib, M, N, K, sms):
+    """Every wait of the split-K fix-up goes from a tile's finisher to the
+    tile's other contributors. The finisher is the CTA for which the tile is its
+    last piece and which holds the tile's first K blocks; every CTA it waits for
+    has a lower block index. Blocks are dispatched in index order, so each CTA
+    waited for is running or done before its waiter starts, and the kernel makes
+    progress even when only some of its CTAs fit on the GPU at once."""
+    plan = sk.gemm_plan(M, N, K, sms)
+    pieces = {c: sk.gemm_cta_pieces(M, N, K, sms, c, max_pieces=plan.tiles + 1)
+              for c in range(plan.ctas)}
+    by_tile = {}
+    for c, ps in pieces.items():
+        for q, (t, kb0, kb1, slot) in enumerate(ps):
+            by_tile.setdefault(t, []).append((c, q, kb0, kb1))
+    edges = 0
+    for t, entries in by_tile.items():
+        if len(entries) == 1:
+            continue
+        finisher = [e for e in entries if e[2] == 0]
+        assert len(finisher) == 1
+        c_fin, q_fin = finisher[0][0], finisher[0][1]
+        assert q_fin == len(pieces[c_fin]) - 1, "a finisher finishes its last piece"
+        for c, q, kb0, kb1 in entries:
+            if c != c_fin:
+                assert c < c_fin, (t, c, c_fin)
+                edges += 1
+    assert (edges > 0) == (plan.split_tiles > 0)
 
 
 def test_l2_prefetch_setting_round_trips_and_rejects_out_of_range(lib):
@@ -324,3 +356,69 @@ def test_default_l2_prefetch_is_six(lib):
                          cwd=os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
     assert out.returncode == 0, out.stderr
     assert out.stdout.strip() == "6"
+
+
+def test_ex_entry_points_validate_options_before_cuda(lib):
+    """The per-call launch settings are checked before anything touches CUDA:
+    a field out of range is SKINNY_ERR_ARG; SKINNY_OPT_DEFAULT (-1) or NULL
+    takes the process-wide setting (here the call then fails for lack of a
+    device, or runs on a GPU machine)."""
+    import torch
+    buf = ctypes.create_string_buffer(1 << 22)
+    p = ctypes.addressof(buf) + (-ctypes.addressof(buf)) % 256
+    bad = [sk.LaunchOpts(2, 0), sk.LaunchOpts(-2, 0), sk.LaunchOpts(1, 65),
+           sk.LaunchOpts(0, -2)]
+    row = 7168 * 2
+    part, res, gam, out, rout = p, p + 8 * row * 2, p + 10 * row * 2, p + 11 * row * 2, \
+        p + 13 * row * 2
+    for o in bad:
+        r = ctypes.byref(o)
+        assert lib.decode_gemm_bf16_ex(p, p + 4096, p + 65536, 4, 16, 64, r, None) == 10
+        assert lib.reduce_residual_rmsnorm_ex(part, 8, res, gam, out, rout, 2, 1e-6, r,
+                                              None) == 10
+        assert lib.decode_gemm_bf16_reduce_rmsnorm_ex(p, p + 65536, p + (2 << 20), 8, None,
+                                                      p + (3 << 20), p + (4 << 20),
+                                                      p + (5 << 20), 2, 64, 1e-6, r, None) == 10
+    if not torch.cuda.is_available():
+        for o in (None, ctypes.byref(sk.LaunchOpts(-1, -1)), ctypes.byref(sk.LaunchOpts(1, 0))):
+            assert lib.decode_gemm_bf16_ex(p, p + 4096, p + 65536, 4, 16, 64, o, None) == 4
+    # Shape errors still come first.
+    assert lib.decode_gemm_bf16_ex(p, p + 4096, p + 65536, 0, 16, 64,
+                                   ctypes.byref(sk.LaunchOpts(1, 0)), None) == 2
+
+
+def test_process_settings_are_thread_safe_and_ex_calls_leave_them(lib):
+    """Two host threads: one flips the process-wide settings, the other makes
+    _ex calls with its own settings. The _ex calls never change the process-wide
+    settings, and the setters stay consistent under contention."""
+    import threading
+    prev_pdl, prev_lead = lib.skinny_set_pdl(0), lib.skinny_set_l2_prefetch(5)
+    stop = threading.Event()
+    seen = []
+
+    def flipper():
+        k = 0
+        while not stop.is_set():
+            lib.skinny_set_pdl(k & 1)
+            lib.skinny_set_l2_prefetch(5)
+            k += 1
+
+    def caller():
+        buf = ctypes.create_string_buffer(1 << 20)
+        p = ctypes.addressof(buf) + (-ctypes.addressof(buf)) % 256
+        o = ctypes.byref(sk.LaunchOpts(1, 64))
+        for _ in range(2000):
+            seen.append(lib.decode_gemm_bf16_ex(p, p + 4096, p + 65536, 0, 16, 64, o, None))
+
+    t1, t2 = threading.Thread(target=flipper), threading.Thread(target=caller)
+    t1.start()
+    t2.start()
+    t2.join()
+    stop.set()
+    t1.join()
+    try:
+        assert set(seen) == {2}
+        assert lib.skinny_set_l2_prefetch(5) == 5  # never the _ex calls' 64
+    finally:
+        lib.skinny_set_pdl(prev_pdl)
+        lib.skinny_set_l2_prefetch(prev_lead)

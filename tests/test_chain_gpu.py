@@ -79,16 +79,12 @@ def test_chain_eager_and_graph_replay_give_the_same_bits(chain_inputs):
     """LayerChain (the benchmark's driver): an eager step with PDL, a second eager
     step and a CUDA-graph replay of the step all produce identical rows."""
     inp = chain_inputs
-    chain = LayerChain(inp.W1, inp.W2, inp.peers, inp.gamma, CFG.M, CFG.eps)
+    chain = LayerChain(inp.W1, inp.W2, inp.peers, inp.gamma, CFG.M, CFG.eps, pdl=True)
     chain.x.copy_(inp.x0)
     chain.res_in.copy_(inp.residual0)
-    prev = sk.set_pdl(True)
-    try:
-        a_out, a_res = (t.clone() for t in chain.run())
-        b_out, b_res = (t.clone() for t in chain.run())
-    finally:
-        sk.set_pdl(prev)
-    g_out, g_res = chain.capture(pdl=True)
+    a_out, a_res = (t.clone() for t in chain.run())
+    b_out, b_res = (t.clone() for t in chain.run())
+    g_out, g_res = chain.capture()
     chain.replay()
     torch.cuda.synchronize()
     for got in (b_out, g_out):
@@ -100,23 +96,27 @@ def test_chain_eager_and_graph_replay_give_the_same_bits(chain_inputs):
 
 def test_fused_chain_equals_unfused_chain(chain_inputs):
     """The chain with decode_gemm_bf16_reduce_rmsnorm for each layer's second GEMM
-    and reduce gives the unfused chain's rows bit for bit (PDL on), whatever the
-    decode GEMM's L2 lead; the chain puts the caller's lead back after a step."""
+    and reduce gives the unfused chain's rows bit for bit, with or without PDL,
+    whatever the decode GEMM's L2 lead; the chain's per-call settings leave the
+    process-wide ones as the caller set them."""
     inp = chain_inputs
     rows = []
-    for fused, lead in ((False, 6), (True, 0), (True, 6), (False, 0)):
+    for fused, lead, pdl in ((False, 6, True), (True, 0, True), (True, 6, False),
+                             (False, 0, False), (True, 0, False)):
         chain = LayerChain(inp.W1, inp.W2, inp.peers, inp.gamma, CFG.M, CFG.eps, fused=fused,
-                           l2_prefetch=lead)
+                           l2_prefetch=lead, pdl=pdl)
         chain.x.copy_(inp.x0)
         chain.res_in.copy_(inp.residual0)
-        prev = sk.set_pdl(True)
+        prev = sk.set_pdl(not pdl)
         prev_lead = sk.set_l2_prefetch(9)
         try:
             out, res = (t.clone() for t in chain.run())
             torch.cuda.synchronize()
             assert sk.set_l2_prefetch(prev_lead) == 9
+            assert sk.set_pdl(prev) == (not pdl)
         finally:
             sk.set_pdl(prev)
+            sk.set_l2_prefetch(prev_lead)
         rows.append((out, res))
     o0, r0 = rows[0]
     for o1, r1 in rows[1:]:

@@ -1,7 +1,9 @@
 """The decode GEMM's bounded waits on the GPU: a wait that can never complete ends
 with a recorded status instead of a hang, the kernel cleans up after itself
-(in-flight copies drained, tensor memory freed), and the context stays usable --
-the next regular call returns the right bits. Nothing here faults or traps."""
+(in-flight copies drained, tensor memory freed), later calls that use the
+split-K scratch report the timeout (SKINNY_ERR_TIMEOUT, nothing launched) until
+the error is read and cleared, and the context stays usable -- the next regular
+call returns the right bits. Nothing here faults or traps."""
 import pytest
 import torch
 
@@ -29,6 +31,18 @@ def test_bounded_wait_reports_and_recovers(cuda_ok, M, N, K):
 
     junk = torch.empty_like(ref)
     sk.watchdog_selftest(x, W, junk, timeout_ns=2_000_000)  # 2 ms limit
+    torch.cuda.synchronize()
+    # The timeout is visible to the host without reading the error word: calls
+    # that would use the scratch refuse to launch.
+    untouched = torch.full_like(ref, 3.0)
+    with pytest.raises(sk.SkinnyError) as e:
+        sk.decode_gemm_bf16(x, W, untouched)
+    assert e.value.status == 9
+    with pytest.raises(sk.SkinnyError) as e:
+        sk.decode_gemm_bf16(x, W, untouched, pdl=True, l2_prefetch=0)
+    assert e.value.status == 9
+    torch.cuda.synchronize()
+    assert bool((untouched.float() == 3.0).all())
     status, word = sk.device_error()
     assert status == 9, sk.status_string(status)
     assert word & SELFTEST_BIT
