@@ -57,6 +57,9 @@ def parse():
     ap.add_argument("--sweep", action="store_true",
                     help="per-config GB/s of every GEMM and reduce config instead of the chain")
     ap.add_argument("--sweep-calls", type=int, default=200)
+    ap.add_argument("--configs", type=int, default=1,
+                    help="add the per-config block (every GEMM / reduce / gather config of "
+                         "the workloads, with the oracle per config kind) to the line")
     ap.add_argument("--profile", action="store_true",
                     help="a few launches of each chain kernel, for ncu captures")
     ap.add_argument("--profile-configs", action="store_true",
@@ -169,6 +172,15 @@ class ClockSampler:
 
 # ---- the oracle as the CPU baseline / reference arm ------------------------------
 
+def host_cores():
+    """Host cores this process may run on: the thread count every all-core oracle
+    timing passes explicitly (OpenMP keeps the last count it was given)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
 def oracle_chain_sample(inp_bits, cfg, cols1, cols2, threads=0):
     """One chain step by the oracle on sampled GEMM output columns. The reduce and
     RMSNorm run on full rows; the sampled columns of GEMM2 fill slot 0 where
@@ -205,15 +217,29 @@ def host_chain_bits(cfg, seed):
             "x0": workloads.bits(inp.x0), "res0": workloads.bits(inp.residual0)}
 
 
-def chain_parity(inp, cfg, sk, samples=512, seed=0):
+def _gemm_literal_report(got_bits, ref, ssum, asum):
+    """The decode GEMM tolerance verdict plus the literal ulp statistics."""
+    from oracle import compare
+    rep = compare.gemm_check(got_bits, ref, ssum, asum)
+    lit = compare.ulp_distance(got_bits, ref)
+    small = np.abs(ssum) < compare.FLOOR_SCALE * asum
+    keep = ("ok", "n", "within1_frac", "max_judged", "below_floor", "literal_hist",
+            "literal_within1_frac", "literal_max")
+    out = {k: rep[k] for k in keep}
+    out["literal_gt2_above_floor"] = int(((lit > 2) & ~small).sum())
+    out["literal_gt2_below_floor"] = int(((lit > 2) & small).sum())
+    return out
+
+
+def chain_parity(inp, cfg, sk):
     """The oracle beside the GPU on the timed chain's own inputs (part of the CPU
-    baseline leg): layer 0's two GEMMs on sampled output columns, with the ulp
-    histogram of the GEMM tolerance, and layer 0's reduce + residual + RMSNorm on
-    whole rows (residual bit for bit, out in ulps)."""
+    baseline leg): every output element of layer 0's two GEMMs, judged by the
+    GEMM tolerance with the literal ulp histogram, and cuBLAS (torch.mm) on the
+    same inputs judged the same way; then layer 0's reduce + residual + RMSNorm
+    on whole rows (residual bit for bit, out in ulps)."""
     import oracle
     from oracle import compare
     dev = inp.x0.device
-    rng = np.random.default_rng(seed)
     h1 = torch.empty(cfg.M, cfg.ffn, dtype=torch.bfloat16, device=dev)
     parts = torch.empty(cfg.TP, cfg.M, cfg.hidden, dtype=torch.bfloat16, device=dev)
     parts[1:].copy_(inp.peers[0])
@@ -222,18 +248,17 @@ def chain_parity(inp, cfg, sk, samples=512, seed=0):
     sk.decode_gemm_bf16(inp.x0, inp.W1[0], h1)
     sk.decode_gemm_bf16(h1, inp.W2[0], parts[0])
     sk.reduce_residual_rmsnorm(parts, inp.residual0, inp.gamma[0], out, rout, cfg.eps)
+    cub1 = torch.mm(inp.x0, inp.W1[0].t())
+    cub2 = torch.mm(h1, inp.W2[0].t())  # the same input as our second GEMM
     torch.cuda.synchronize()
-    report = {}
-    for name, x, W, y in (("gemm1", inp.x0, inp.W1[0], h1), ("gemm2", h1, inp.W2[0], parts[0])):
-        cols = np.sort(rng.choice(W.shape[0], size=min(samples, W.shape[0]), replace=False))
-        wsel = workloads.bits(W[torch.as_tensor(cols, device=dev, dtype=torch.long)])
-        xb = workloads.bits(x)
-        idx = np.arange(cols.size, dtype=np.int32)
-        ref = oracle.decode_gemm(xb, wsel, cols=idx)
-        ssum, asum = oracle.decode_gemm_f64(xb, wsel, cols=idx)
-        rep_ = compare.gemm_check(workloads.bits(y)[:, cols], ref, ssum, asum)
-        report[name] = {k: rep_[k] for k in ("ok", "n", "within1_frac", "max_judged",
-                                             "literal_hist", "literal_max")}
+    report = {"gemm_columns": "all"}
+    for name, x, W, y, c in (("gemm1", inp.x0, inp.W1[0], h1, cub1),
+                             ("gemm2", h1, inp.W2[0], parts[0], cub2)):
+        xb, wb = workloads.bits(x), workloads.bits(W)
+        ref = oracle.decode_gemm(xb, wb)
+        ssum, asum = oracle.decode_gemm_f64(xb, wb)
+        report[name] = _gemm_literal_report(workloads.bits(y), ref, ssum, asum)
+        report[name + "_cublas"] = _gemm_literal_report(workloads.bits(c), ref, ssum, asum)
     want_h = oracle.reduce_residual(workloads.bits(parts), workloads.bits(inp.residual0))
     want_o = oracle.rmsnorm(want_h, workloads.bits(inp.gamma[0]), cfg.eps)
     d = compare.ulp_distance(workloads.bits(out), want_o)
@@ -253,7 +278,7 @@ def time_oracle(cfg, budget_s, steps=None, warmup=0, seed=0, threads=None):
     from oracle import build as obuild
     obuild.build()
     bits = host_chain_bits(cfg, seed)
-    threads = oracle.max_threads() if threads is None else threads
+    threads = host_cores() if threads is None else threads
     probe = 64
     t0 = time.perf_counter()
     oracle_chain_sample(bits, cfg, np.arange(probe), np.arange(probe), threads)
@@ -341,19 +366,31 @@ def _time_calls(fn, calls, copies, stream):
     return statistics.median(times)
 
 
-def run_sweep(args):
-    import __graft_entry__
-    __graft_entry__.build()
-    import skinny_bf16_gemm_gb300 as sk
-    sk.set_pdl(bool(args.pdl))
-    dev = torch.device("cuda", 0)
+GATHER_CONFIGS = [(8, m, 896) for m in (1, 16, 64)] + [(8, m, 2560) for m in (1, 8, 32, 64)]
+
+
+def _entry(peak, nb, t_ms, **fields):
+    gbs = nb / (t_ms * 1e-3) / 1e9
+    fields.update({"us": t_ms * 1e3, "GBps": gbs, "frac_measured": gbs / peak,
+                   "frac_nominal_8000": gbs / 8000.0, "bytes": nb})
+    return fields
+
+
+def measure_configs(sk, calls, peak):
+    """Per-call time of every GEMM, reduce and gather config (PR1, the reduce
+    sweep with and without residual, the GEMM sweep, lm_head, the wider shapes,
+    the chain's two GEMMs and the local gather), each from a CUDA graph of
+    `calls` back-to-back calls rotating through buffer copies that span at least
+    3x L2 (median of 5 replays); cuBLAS (torch.mm) timed the same way beside
+    every GEMM."""
+    dev = torch.device("cuda", torch.cuda.current_device())
     stream = torch.cuda.current_stream()
-    peak, peak_kind = measured_peaks()
-    results = []
-    gemms = ([("pr1", workloads.PR1_GEMM)] + [("sweep", g) for g in workloads.GEMM_SWEEP]
+    out_sets = {"pr1": {}, "gemm_sweep": [], "lm_head": [], "wider": [], "chain_gemms": [],
+                "reduce_sweep": [], "gather": []}
+    gemms = ([("pr1", workloads.PR1_GEMM)] + [("gemm_sweep", g) for g in workloads.GEMM_SWEEP]
              + [("lm_head", g) for g in workloads.LM_HEAD]
              + [("wider", g) for g in workloads.GEMM_WIDER]
-             + [("chain", workloads.CHAIN.gemm1()), ("chain", workloads.CHAIN.gemm2())])
+             + [("chain_gemms", workloads.CHAIN.gemm1()), ("chain_gemms", workloads.CHAIN.gemm2())])
     for label, g in gemms:
         copies = _rotation(g.weight_bytes())
         gen = torch.Generator(device=dev)
@@ -362,20 +399,18 @@ def run_sweep(args):
               for _ in range(copies)]
         x = torch.randn(g.M, g.K, device=dev, generator=gen).to(torch.bfloat16)
         out = torch.empty(g.M, g.N, device=dev, dtype=torch.bfloat16)
-        ours = _time_calls(lambda i: sk.decode_gemm_bf16(x, Ws[i], out), args.sweep_calls,
-                           copies, stream)
-        cub = _time_calls(lambda i: torch.mm(x, Ws[i].t(), out=out), args.sweep_calls, copies,
-                          stream)
+        ours = _time_calls(lambda i: sk.decode_gemm_bf16(x, Ws[i], out), calls, copies, stream)
+        cub = _time_calls(lambda i: torch.mm(x, Ws[i].t(), out=out), calls, copies, stream)
         nb = g.algorithmic_bytes()
-        results.append({"kind": "decode_gemm", "set": label, "M": g.M, "N": g.N, "K": g.K,
-                        "us": ours * 1e3, "GBps": nb / (ours * 1e-3) / 1e9,
-                        "frac_measured": nb / (ours * 1e-3) / 1e9 / peak,
-                        "frac_nominal_8000": nb / (ours * 1e-3) / 1e9 / 8000.0,
-                        "cublas_us": cub * 1e3, "cublas_GBps": nb / (cub * 1e-3) / 1e9,
-                        "rotation_copies": copies})
+        e = _entry(peak, nb, ours, M=g.M, N=g.N, K=g.K, cublas_us=cub * 1e3,
+                   cublas_GBps=nb / (cub * 1e-3) / 1e9, rotation_copies=copies)
+        if label == "pr1":
+            out_sets["pr1"]["gemm"] = e
+        else:
+            out_sets[label].append(e)
         del Ws
         torch.cuda.empty_cache()
-    reduces = [("pr1", workloads.PR1_REDUCE)] + [("sweep", r) for r in workloads.REDUCE_SWEEP]
+    reduces = [("pr1", workloads.PR1_REDUCE)] + [("reduce_sweep", r) for r in workloads.REDUCE_SWEEP]
     for label, r in reduces:
         per = 2 * r.width * r.M * (r.TP + 1)
         copies = _rotation(per)
@@ -387,28 +422,138 @@ def run_sweep(args):
         out = torch.empty(r.M, r.width, device=dev, dtype=torch.bfloat16)
         rout = torch.empty_like(out)
         t = _time_calls(lambda i: sk.reduce_residual_rmsnorm(parts[i], ress[i], gamma, out, rout),
-                        args.sweep_calls, copies, stream)
-        nb = r.algorithmic_bytes()
-        results.append({"kind": "reduce_rmsnorm", "set": label, "TP": r.TP, "M": r.M,
-                        "residual": r.residual, "us": t * 1e3, "GBps": nb / (t * 1e-3) / 1e9,
-                        "frac_measured": nb / (t * 1e-3) / 1e9 / peak, "rotation_copies": copies})
+                        calls, copies, stream)
+        e = _entry(peak, r.algorithmic_bytes(), t, TP=r.TP, M=r.M, residual=r.residual,
+                   rotation_copies=copies)
+        if label == "pr1":
+            out_sets["pr1"]["reduce"] = e
+        else:
+            out_sets[label].append(e)
         del parts, ress
         torch.cuda.empty_cache()
-    for TP, M, S in ([(8, m, 896) for m in (1, 16, 64)] + [(8, m, 2560) for m in (1, 8, 32, 64)]):
+    for TP, M, S in GATHER_CONFIGS:
         per = 2 * TP * M * S
         copies = _rotation(per)
         shards = [torch.randn(TP, M, S, device=dev).to(torch.bfloat16) for _ in range(copies)]
         out = torch.empty(M, TP * S, device=dev, dtype=torch.bfloat16)
-        t = _time_calls(lambda i: sk.gather_shards_bf16(shards[i], out), args.sweep_calls, copies,
-                        stream)
-        nb = 2 * per  # read every shard once, write the gathered rows once
-        results.append({"kind": "gather", "set": "context" if S == 896 else "logits", "TP": TP,
-                        "M": M, "S": S, "us": t * 1e3, "GBps": nb / (t * 1e-3) / 1e9,
-                        "frac_measured": nb / (t * 1e-3) / 1e9 / peak, "rotation_copies": copies})
+        t = _time_calls(lambda i: sk.gather_shards_bf16(shards[i], out), calls, copies, stream)
+        out_sets["gather"].append(_entry(peak, 2 * per, t, TP=TP, M=M, S=S,
+                                         set="context" if S == 896 else "logits",
+                                         rotation_copies=copies))
         del shards
         torch.cuda.empty_cache()
-    print(json.dumps({"sweep": results, "peak_gbs": peak, "peak_source": peak_kind,
-                      "pdl": bool(args.pdl), "calls_per_config": args.sweep_calls}), flush=True)
+    return out_sets
+
+
+def oracle_configs(budget_s=2.0, seed=0):
+    """The oracle timed on the host cores on each config kind of the report:
+    PR1's GEMM and reduce whole, the reduce sweep and the gathers whole, the
+    GEMM sweep, lm_head and wider shapes on sampled output columns (the bytes
+    counted are those of the sample). Each kind repeats for about budget_s."""
+    import oracle
+    threads = host_cores()
+    rng = np.random.default_rng(seed)
+
+    def gemm_job(shapes, cols):
+        jobs = []
+        for g in shapes:
+            n = min(cols, g.N)
+            inp = workloads.gemm_inputs(g.M, n, g.K, workloads.seed_for("oracle-cfg", g.M, g.N, g.K))
+            jobs.append((workloads.bits(inp.x), workloads.bits(inp.W),
+                         2 * n * g.K + 2 * g.M * g.K + 2 * g.M * n))
+        def run():
+            nb = 0
+            for xb, wb, b in jobs:
+                oracle.decode_gemm(xb, wb, threads=threads)
+                nb += b
+            return nb
+        every = all(cols >= g.N for g in shapes)
+        what = "all output columns" if every else f"{cols} output columns each"
+        return run, f"{len(shapes)} shape(s), {what}", threads
+
+    def reduce_job(shapes):
+        jobs = []
+        for r in shapes:
+            inp = workloads.reduce_inputs(r.TP, r.M, workloads.seed_for("oracle-cfg", r.TP, r.M),
+                                          r.residual)
+            jobs.append((workloads.bits(inp.partials),
+                         None if inp.residual is None else workloads.bits(inp.residual),
+                         workloads.bits(inp.gamma), r.algorithmic_bytes()))
+        def run():
+            nb = 0
+            for p, res, gam, b in jobs:
+                oracle.reduce_residual_rmsnorm(p, res, gam, 1e-6)
+                nb += b
+            return nb
+        return run, f"{len(shapes)} config(s), whole rows (single-threaded oracle)", 1
+
+    def gather_job():
+        jobs = [(rng.integers(0, 1 << 16, size=(TP, M, S), dtype=np.uint16), 4 * TP * M * S)
+                for TP, M, S in GATHER_CONFIGS]
+        def run():
+            nb = 0
+            for sh, b in jobs:
+                oracle.gather_shards(sh)
+                nb += b
+            return nb
+        return run, f"{len(GATHER_CONFIGS)} config(s), whole rows (single-threaded oracle)", 1
+
+    kinds = {
+        "pr1_gemm": gemm_job([workloads.PR1_GEMM], 1 << 30),
+        "pr1_reduce": reduce_job([workloads.PR1_REDUCE]),
+        "reduce_sweep": reduce_job(workloads.REDUCE_SWEEP),
+        "gemm_sweep": gemm_job(workloads.GEMM_SWEEP, 64),
+        "lm_head": gemm_job(workloads.LM_HEAD, 256),
+        "wider": gemm_job(workloads.GEMM_WIDER, 64),
+        "gather": gather_job(),
+    }
+    out = {}
+    for name, (run, sample, cores) in kinds.items():
+        run()  # warm
+        nb, reps, t0 = 0, 0, time.perf_counter()
+        while True:
+            nb += run()
+            reps += 1
+            dt = time.perf_counter() - t0
+            if dt >= budget_s:
+                break
+        out[name] = {"GBps": nb / dt / 1e9, "cores": cores, "kind": "oracle",
+                     "sample": f"{sample}; {reps} pass(es) in {dt:.2f} s"}
+    return out
+
+
+def configs_report(sk, calls, peak, peak_kind, device_index, pdl=True, with_oracle=True):
+    """The per-config block of the benchmark line: GPU per-call figures under a
+    clock record, with the oracle's GB/s per config kind beside them."""
+    clocks = ClockSampler(device_index)
+    prev = sk.set_pdl(pdl)
+    try:
+        clocks.start()
+        time.sleep(0.3)
+        sets = measure_configs(sk, calls, peak)
+        torch.cuda.synchronize()
+    finally:
+        sk.set_pdl(prev)
+    sets["clocks"] = clocks.stop()
+    sets["peak_gbs"] = peak
+    sets["peak_source"] = peak_kind
+    sets["timing"] = (f"CUDA graph of {calls} back-to-back calls per config rotating through "
+                      "buffer copies spanning >= 3x L2, median of 5 replays, CUDA events; "
+                      f"PDL {'on' if pdl else 'off'}")
+    if with_oracle:
+        sets["oracle"] = oracle_configs()
+    return sets
+
+
+def run_sweep(args):
+    import __graft_entry__
+    __graft_entry__.build()
+    import skinny_bf16_gemm_gb300 as sk
+    peak, peak_kind = measured_peaks()
+    rep = configs_report(sk, args.sweep_calls, peak, peak_kind, torch.cuda.current_device(),
+                         pdl=bool(args.pdl), with_oracle=not args.no_cpu_baseline)
+    rep["calls_per_config"] = args.sweep_calls
+    print(json.dumps({"configs": rep}), flush=True)
     return 0
 
 
@@ -452,7 +597,7 @@ def run_profile_configs(args):
             sk.reduce_residual_rmsnorm(inp.partials, inp.residual, inp.gamma, out, rout, 1e-6)
         torch.cuda.synchronize()
         labels.append({"label": name, "kernel": "reduce_rmsnorm", "bytes": r.algorithmic_bytes()})
-    for TP, M, S in ([(8, m, 896) for m in (1, 16, 64)] + [(8, m, 2560) for m in (1, 8, 32, 64)]):
+    for TP, M, S in GATHER_CONFIGS:
         name = f"gather TP={TP} M={M} S={S}"
         if args.config_filter not in name:
             continue
@@ -528,7 +673,8 @@ def main():
     from skinny_bf16_gemm_gb300.replicas import replica_seed
     inp = workloads.chain_inputs(cfg, replica_seed(workloads.seed_for("chain"), rank), device=device)
     chain = LayerChain(inp.W1, inp.W2, inp.peers, inp.gamma, cfg.M, cfg.eps, device=device,
-                       fused=bool(args.fused), l2_prefetch=args.l2_prefetch)
+                       fused=bool(args.fused), l2_prefetch=args.l2_prefetch,
+                       pdl=bool(args.pdl))
     chain.x.copy_(inp.x0)
     chain.res_in.copy_(inp.residual0)
     sk.set_pdl(bool(args.pdl))
@@ -547,7 +693,7 @@ def main():
         chain.run()
     torch.cuda.synchronize()
     if args.graph:
-        chain.capture(pdl=bool(args.pdl))
+        chain.capture()
         for _ in range(3):
             chain.replay()
         torch.cuda.synchronize()
@@ -586,16 +732,20 @@ def main():
     # launch would serialise the kernels and add each launch's gap.
     kernel_steps = max(1, min(args.steps, 400))
 
+    # The chain's launch settings, passed with every call.
+    kopts = dict(pdl=bool(args.pdl), l2_prefetch=args.l2_prefetch)
+
     def gemm_only():
         x = chain.x
         for l in range(cfg.layers):
-            sk.decode_gemm_bf16(x, chain.W1[l], chain.h1)
-            sk.decode_gemm_bf16(chain.h1, chain.W2[l], chain.partials[l][0])
+            sk.decode_gemm_bf16(x, chain.W1[l], chain.h1, **kopts)
+            sk.decode_gemm_bf16(chain.h1, chain.W2[l], chain.partials[l][0], **kopts)
 
     def reduce_only():
         for l in range(cfg.layers):
             sk.reduce_residual_rmsnorm(chain.partials[l], chain.res_in, chain.gamma[l],
-                                       chain.outs[l % 2], chain.res[l % 2], cfg.eps)
+                                       chain.outs[l % 2], chain.res[l % 2], cfg.eps,
+                                       pdl=kopts["pdl"])
 
     def loop_ms(fn, reps):
         for _ in range(3):
@@ -630,11 +780,7 @@ def main():
         return e0.elapsed_time(e1)
 
     gemm_launches = kernel_steps * 2 * cfg.layers
-    prev_lead = sk.set_l2_prefetch(args.l2_prefetch)  # as the chain runs its GEMMs
-    try:
-        gemm_ms = loop_ms(gemm_only, kernel_steps) / gemm_launches
-    finally:
-        sk.set_l2_prefetch(prev_lead)
+    gemm_ms = loop_ms(gemm_only, kernel_steps) / gemm_launches
     reduce_reps = 100
     reduce_ms = graph_ms(reduce_only, reduce_reps) / (reduce_reps * cfg.layers)
     g1 = cfg.gemm1()
@@ -662,7 +808,7 @@ def main():
     e2e_steps = max(G, min(args.steps, 500)) // G * G
     chains = [chain] + [LayerChain(inp.W1, inp.W2, inp.peers, inp.gamma, cfg.M, cfg.eps,
                                    device=device, fused=bool(args.fused),
-                                   l2_prefetch=args.l2_prefetch)
+                                   l2_prefetch=args.l2_prefetch, pdl=bool(args.pdl))
                         for _ in range(2 * G - 1)]
     copy_stream = torch.cuda.Stream()
     inputs_ready = [torch.cuda.Event() for _ in range(2)]
@@ -750,6 +896,10 @@ def main():
         one = time_oracle(cfg, 5.0, threads=1)
         line["cpu_baseline"]["one_thread"] = {"value": one["value"], "sample": one["sample"]}
         line["parity"] = chain_parity(inp, cfg, sk)
+    if rank == 0 and args.configs:
+        line["configs"] = configs_report(sk, args.sweep_calls, peak, peak_kind, local,
+                                         pdl=bool(args.pdl),
+                                         with_oracle=world == 1 and not args.no_cpu_baseline)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
