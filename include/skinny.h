@@ -107,7 +107,8 @@ typedef struct {
  *        aligned. Read exactly once from HBM.
  *   out  [M, N] BF16, row-major (row stride N elements), 2-byte aligned. Written
  *        once; must not overlap x or W.
- *   1 <= M <= 64;  N >= 1;  K >= 8 and K % 8 == 0 (16-byte row strides).
+ *   1 <= M <= 64;  N >= 1;  K >= 8 and K % 8 == 0 (16-byte row strides);
+ *   ceil(N / 128) * ceil(K / 64) < 2^31 (a weight below 32 TiB).
  *   Ragged N (N % 128 != 0) and ragged K (K % 64 != 0) are handled exactly.
  *
  *   Every out element is the FP32 sum of the K products (split over K across

@@ -182,6 +182,11 @@ int encode_2d(EncodeTiledFn enc, CUtensorMap *map, const void *base, uint64_t ro
 
 int gemm_shape_ok(int M, int N, int K) {
     if (M < 1 || M > kMaxM || N < 1 || K < 8 || (K % 8) != 0) return SKINNY_ERR_SHAPE;
+    // The kernel counts 128 x 64 weight blocks in 32-bit integers (a weight of
+    // 2^31 blocks would be 32 TiB).
+    const long long blocks = static_cast<long long>((N + kBlockN - 1) / kBlockN) *
+                             ((K + kBlockK - 1) / kBlockK);
+    if (blocks >= (1ll << 31)) return SKINNY_ERR_SHAPE;
     return SKINNY_OK;
 }
 

@@ -198,9 +198,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     // anything it writes.
     ptx::pdl_launch_dependents();
 
-    const int pieces = cta_piece_count(g, cta);
+    // This CTA's blocks [b0, b1). Block indices stay below 2^31 (the host rejects
+    // larger problems), so after the two 64-bit divisions of the range ends all
+    // the plan arithmetic here is 32-bit.
     const long long b0 = cta_begin(g, cta);
-    const long long total = cta_begin(g, cta + 1) - b0;
+    const long long b1 = cta_begin(g, cta + 1);
+    const int total = static_cast<int>(b1 - b0);
+    const BlockCursor start = {static_cast<int>(b0) / g.kblocks,
+                               static_cast<int>(b0) - (static_cast<int>(b0) / g.kblocks) * g.kblocks};
+    const int pieces = total > 0 ? (static_cast<int>(b1) - 1) / g.kblocks - start.t + 1 : 0;
+    // Piece q of this CTA's range (plan.cuh cta_piece, from the range ends above).
+    auto piece_of = [&](int q) {
+        Piece p;
+        p.tile = start.t + q;
+        const int t0 = p.tile * g.kblocks;
+        p.kb0 = static_cast<int>(b0) > t0 ? static_cast<int>(b0) - t0 : 0;
+        p.kb1 = (static_cast<int>(b1) < t0 + g.kblocks ? static_cast<int>(b1) : t0 + g.kblocks) - t0;
+        return p;
+    };
 
     // Producer bookkeeping kept for the drain (lane 0 of warp 0).
     uint32_t armed = 0, armed_parity = 0;
@@ -214,48 +229,46 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::prefetch_tensormap(&x_map);
             const uint64_t pol_w = ptx::policy_evict_first();
             const uint64_t pol_x = ptx::policy_evict_last();
-            const int npre = static_cast<int>(total < S ? total : S);
+            const int npre = total < S ? total : S;
             // Fresh stages: arm them and stream weights before the predecessor ends.
+            BlockCursor w = start;
             for (int j = 0; j < npre; ++j) {
-                const long long blk = b0 + j;
-                const int t = static_cast<int>(blk / g.kblocks);
-                const int kb = static_cast<int>(blk % g.kblocks);
                 const uint32_t st = sbase + j * L::kStageBytes;
                 ptx::mbar_arrive_expect_tx(bar_full + 8 * j, L::kStageBytes);
                 armed |= 1u << j;
-                ptx::tma_load_2d(st, &w_map, bar_full + 8 * j, kb * kBlockK, t * kBlockN, pol_w);
+                ptx::tma_load_2d(st, &w_map, bar_full + 8 * j, w.kb * kBlockK, w.t * kBlockN, pol_w);
+                w.next(g.kblocks);
             }
             // The blocks after the ring's worth go to L2 ahead of time.
-            const long long lead = STAGES <= kMaxShallowStages ? kL2PrefetchShallow : args.l2_lead;
-            const long long npf = total - npre < lead ? total - npre : lead;
-            for (long long j = npre; j < npre + npf; ++j) {
-                const long long blk = b0 + j;
-                ptx::tma_prefetch_l2_2d(&w_map, static_cast<int>(blk % g.kblocks) * kBlockK,
-                                        static_cast<int>(blk / g.kblocks) * kBlockN);
+            const int lead = STAGES <= kMaxShallowStages ? kL2PrefetchShallow : args.l2_lead;
+            const int npf = total - npre < lead ? total - npre : lead;
+            BlockCursor pf = w;
+            for (int j = 0; j < npf; ++j) {
+                ptx::tma_prefetch_l2_2d(&w_map, pf.kb * kBlockK, pf.t * kBlockN);
+                pf.next(g.kblocks);
             }
             ptx::pdl_wait();  // x may be the predecessor's output
+            BlockCursor xc = start;
             for (int j = 0; j < npre; ++j) {
-                const int kb = static_cast<int>((b0 + j) % g.kblocks);
                 const uint32_t st = sbase + j * L::kStageBytes;
-                ptx::tma_load_2d(st + kWBytes, &x_map, bar_full + 8 * j, kb * kBlockK, 0, pol_x);
+                ptx::tma_load_2d(st + kWBytes, &x_map, bar_full + 8 * j, xc.kb * kBlockK, 0, pol_x);
+                xc.next(g.kblocks);
             }
             int s = npre % S;
             uint32_t ph = npre == S ? 1u : 0u;
-            for (long long j = npre; j < total; ++j) {
+            for (int j = npre; j < total; ++j) {
                 const int r = bounded_wait(bar_empty + 8 * s, ph ^ 1u, abort_flag, limit);
                 if (r != kWaitDone) {
                     if (r == kWaitTimeout) raise_error(args, abort_flag, kErrProducerWait);
                     break;
                 }
-                const long long blk = b0 + j;
-                const int t = static_cast<int>(blk / g.kblocks);
-                const int kb = static_cast<int>(blk % g.kblocks);
                 const uint32_t st = sbase + s * L::kStageBytes;
                 ptx::mbar_arrive_expect_tx(bar_full + 8 * s, L::kStageBytes);
                 armed |= 1u << s;
                 armed_parity = (armed_parity & ~(1u << s)) | (ph << s);
-                ptx::tma_load_2d(st, &w_map, bar_full + 8 * s, kb * kBlockK, t * kBlockN, pol_w);
-                ptx::tma_load_2d(st + kWBytes, &x_map, bar_full + 8 * s, kb * kBlockK, 0, pol_x);
+                ptx::tma_load_2d(st, &w_map, bar_full + 8 * s, w.kb * kBlockK, w.t * kBlockN, pol_w);
+                ptx::tma_load_2d(st + kWBytes, &x_map, bar_full + 8 * s, w.kb * kBlockK, 0, pol_x);
+                w.next(g.kblocks);
                 if (++s == S) {
                     s = 0;
                     ph ^= 1u;
@@ -278,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = false;
             }
             for (int q = 0; ok && q < pieces; ++q) {
-                const Piece p = cta_piece(g, cta, q);
+                const Piece p = piece_of(q);
                 const int b = q & 1;
                 const uint32_t aph = (q >> 1) & 1;
                 int r = bounded_wait(bar_acc_empty + 8 * b, aph ^ 1u, abort_flag, limit);
@@ -401,12 +414,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
 
         for (int q = 0; q < pieces; ++q) {
-            const Piece p = cta_piece(g, cta, q);
+            const Piece p = piece_of(q);
             // The plan's arithmetic (64-bit divisions) before the wait, not on
             // the split-K tail after it.
             int first, last;
             tile_contributors(g, p.tile, first, last);
-            const int my_slot = partial_slot(g, cta, p.tile);
+            const int my_slot = 2 * cta + (p.tile == start.t ? 0 : 1);  // plan.cuh partial_slot
             const int first_peer_slot =
                 first + 1 + etid <= last ? partial_slot(g, first + 1 + etid, p.tile) : 0;
             const int b = q & 1;

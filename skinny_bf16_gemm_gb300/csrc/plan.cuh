@@ -119,6 +119,18 @@ __host__ __device__ inline Piece cta_piece(const GemmGeometry &g, int c, int q) 
     return p;
 }
 
+// A walk over consecutive weight blocks in tile-major order without divisions
+// (64-bit integer division is a long software sequence on the GPU).
+struct BlockCursor {
+    int t, kb;  // tile, K block within it
+    __host__ __device__ void next(int kblocks) {
+        if (++kb == kblocks) {
+            kb = 0;
+            ++t;
+        }
+    }
+};
+
 // Ranges contributing to tile t, in K order: [first, last].
 __host__ __device__ inline void tile_contributors(const GemmGeometry &g, int t, int &first,
                                                   int &last) {

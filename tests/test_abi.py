@@ -422,3 +422,14 @@ def test_process_settings_are_thread_safe_and_ex_calls_leave_them(lib):
     finally:
         lib.skinny_set_pdl(prev_pdl)
         lib.skinny_set_l2_prefetch(prev_lead)
+
+
+def test_gemm_rejects_block_counts_beyond_32_bits(lib):
+    """The kernel counts 128 x 64 weight blocks in 32-bit integers: a shape with
+    2^31 blocks or more is rejected before anything else happens."""
+    buf = ctypes.create_string_buffer(1 << 16)
+    p = ctypes.addressof(buf) + (-ctypes.addressof(buf)) % 256
+    N, K = 2 ** 31 - 128, 2 ** 20 * 8  # ceil(N/128) * ceil(K/64) >= 2^31
+    assert lib.decode_gemm_bf16(p, p + 8192, p + 16384, 4, N, K, None) == 2
+    plan = sk.GemmPlan()
+    assert lib.skinny_gemm_plan_query(4, N, K, 152, ctypes.byref(plan)) == 2
