@@ -287,7 +287,7 @@ int gemm_launch(const void *x, const void *W, void *out, int M, int N, int K, vo
         cudaError_t e = launch_decode_gemm(w_map, x_map, a, mma_n, g.ctas, s, pdl,
                                            use_shallow_ring(g, pdl), dev);
         if (e == cudaSuccess) {
-            SplitKPartials fix;
+            SplitKPartials fix = {};
             fix.partials = d->partials;
             fix.slot_floats = kSlotFloats;
             fix.M = M;
@@ -482,7 +482,7 @@ int decode_gemm_bf16_reduce_rmsnorm_ex(const void *x, const void *W, void *parti
         cudaGetLastError();
         return SKINNY_ERR_LAUNCH;
     }
-    SplitKPartials fix;
+    SplitKPartials fix = {};
     fix.partials = d->partials;
     fix.slot_floats = kSlotFloats;
     fix.M = M;
