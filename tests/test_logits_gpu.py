@@ -38,7 +38,8 @@ def check(x, W_rows, got, cap, scale):
 
 @pytest.mark.parametrize("M,N,K,n_out,cap,scale", [
     (4, 1000, 7168, 900, 30.0, 0.5), (16, 300, 200, 300, 0.0, 2.0), (1, 129, 72, 100, 1.0, 1.0),
-    (32, 512, 1024, 512, 5.0, -0.25), (64, 257, 520, 250, 30.0, 1.0)])
+    (32, 512, 1024, 512, 5.0, -0.25), (64, 257, 520, 250, 30.0, 1.0),
+    (8, 2048, 7168, 2000, 30.0, 0.5)])  # the last one runs the cluster plan on a GB300
 def test_logits_small_full(cuda_ok, M, N, K, n_out, cap, scale):
     x, W = gemm_inputs_device(M, N, K, workloads.seed_for("logits", M, N, K))
     x = (x.float() * 8).to(torch.bfloat16)  # logits of a few units: the cap bends them
