@@ -87,6 +87,27 @@ __global__ void __launch_bounds__(ReduceShape<C>::kThreads)
     if (active) gw = __ldg(gamma + frag);
     // The next kernel may launch now: a decode GEMM that follows sets up and
     // streams its first weights while this kernel waits and runs.
+    // FIX: the plan arithmetic of this thread's tile (64-bit divisions) and the
+    // addresses of its first partials before the wait, off the path from the
+    // GEMM's end to this kernel's first load (measured on GB300: the layer
+    // chain's step 1.6 us faster). Up to kU contributors' partials are loaded
+    // together (fewer with 896-thread CTAs, whose register budget is smaller).
+    constexpr int kU = C == 1 ? 2 : 4;
+    int fx_first = 0, fx_last = -1, fx_t = 0;
+    const float *fx_src[kU];
+    GemmGeometry fx_g = {};
+    if constexpr (FIX) {
+        fx_g = make_geometry(fix.M, fix.N, fix.K, fix.ctas);
+        const int col = frag * 8;
+        fx_t = col / kBlockN;
+        tile_contributors(fx_g, fx_t, fx_first, fx_last);
+#pragma unroll
+        for (int q = 0; q < kU; ++q)
+            fx_src[q] = fx_first + q <= fx_last
+                            ? fix.partials + static_cast<size_t>(partial_slot(fx_g, fx_first + q, fx_t)) * fix.slot_floats +
+                                  row * kBlockN + (col % kBlockN)
+                            : nullptr;
+    }
     ptx::pdl_launch_dependents();
     ptx::pdl_wait();  // the partial rows may be the previous kernel's output
 
@@ -103,14 +124,10 @@ __global__ void __launch_bounds__(ReduceShape<C>::kThreads)
 
         float s[8];
         if constexpr (FIX) {
-            const GemmGeometry g = make_geometry(fix.M, fix.N, fix.K, fix.ctas);
+            const GemmGeometry &g = fx_g;
             const int col = frag * 8;
-            const int t = col / kBlockN;
-            int first, last;
-            tile_contributors(g, t, first, last);
-            // Partials of up to kU contributors in flight together (fewer with
-            // 896-thread CTAs, whose register budget is smaller).
-            constexpr int kU = C == 1 ? 2 : 4;
+            const int t = fx_t;
+            const int first = fx_first, last = fx_last;
             float a[8];
             for (int c0 = first; c0 <= last; c0 += kU) {
                 float4 v[kU][2];
@@ -118,8 +135,9 @@ __global__ void __launch_bounds__(ReduceShape<C>::kThreads)
                 for (int q = 0; q < kU; ++q) {
                     if (c0 + q <= last) {
                         const float4 *src = reinterpret_cast<const float4 *>(
-                            fix.partials + static_cast<size_t>(partial_slot(g, c0 + q, t)) * fix.slot_floats +
-                            row * kBlockN + (col % kBlockN));
+                            c0 == first ? fx_src[q]
+                                        : fix.partials + static_cast<size_t>(partial_slot(g, c0 + q, t)) * fix.slot_floats +
+                                              row * kBlockN + (col % kBlockN));
                         v[q][0] = __ldcg(src);
                         v[q][1] = __ldcg(src + 1);
                     }
