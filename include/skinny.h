@@ -285,7 +285,8 @@ SKINNY_API const char *skinny_status_string(int status);
  *   Synchronises the device, then returns SKINNY_OK if no kernel of this library
  *   recorded a problem since the last read, else SKINNY_ERR_TIMEOUT, and writes
  *   the raw word (a bit set per waiting role that gave up; 64 if only the
- *   host-mapped word was set) to *word if word is not NULL. Clearing also
+ *   host-mapped word was set; 128 if a reduce_residual_rmsnorm cluster's
+ *   exchange of its sums of squares ran out) to *word if word is not NULL. Clearing also
  *   re-arms the decode GEMM's scratch flags, so the next call starts clean and
  *   calls stop returning SKINNY_ERR_TIMEOUT. Host pointer: word.
  */

@@ -647,6 +647,13 @@ int skinny_device_error(int device, int *word) {
             }
         }
     }
+    // The reduce kernel's own word (its cluster exchange waits).
+    int reduce_word = 0;
+    if (st == SKINNY_OK && reduce_error_word(&reduce_word, true) != cudaSuccess) {
+        cudaGetLastError();
+        st = SKINNY_ERR_DEVICE;
+    }
+    if (reduce_word) value |= kErrReduceExchange;
     cudaSetDevice(prev);
     if (word) *word = value;
     if (st != SKINNY_OK) return st;

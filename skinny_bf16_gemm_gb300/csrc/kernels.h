@@ -16,6 +16,7 @@ enum ErrorBits : int {
     kErrDrain = 16,         // teardown: in-flight copies or MMAs did not finish
     kErrSelftest = 32,      // the watchdog self-test's deliberate wait ran out
     kErrUnknown = 64,       // the host-mapped word was set but the device word was not
+    kErrReduceExchange = 128,  // reduce: a cluster exchange wait ran out
 };
 
 struct GemmArgs {
@@ -100,6 +101,10 @@ cudaError_t launch_reduce_rmsnorm_splitk(void *partials, int TP, const void *res
                                          const void *gamma, void *out, void *residual_out, int M,
                                          float eps, int ctas_per_row, const SplitKPartials &fix,
                                          cudaStream_t stream, bool pdl);
+
+// The reduce kernel's own error word on the current device (nonzero: a
+// cluster exchange wait ran out), cleared after reading if `clear`.
+cudaError_t reduce_error_word(int *value, bool clear);
 
 // Gather TP shards [TP, M, S] into rows [M, TP * S] (S a multiple of 8).
 cudaError_t launch_gather(const void *shards, int TP, int M, int S, void *out,

@@ -13,7 +13,12 @@
 // fragment, so a whole row's TP + 1 loads per thread are in flight at once. The
 // row's sum of squares: an FMA chain over the thread's 8 values, a warp butterfly,
 // the warps in order, then the C CTA sums exchanged through distributed shared
-// memory and added in CTA order (every CTA gets the same bits).
+// memory and added in CTA order (every CTA gets the same bits). Each CTA sends its
+// sum to every peer with st.async, which completes bytes on the peer's mbarrier,
+// and waits on its own: measured on GB300, 0.3-0.4 us faster per call than
+// remote stores followed by a full cluster barrier (the layer chain's step
+// 1.5 us faster). The wait is bounded; one that runs out is recorded in a
+// device word skinny_device_error() reports.
 // With programmatic dependent launch, gamma (a weight) is loaded before waiting
 // for the previous kernel; the partial rows and the residual after.
 #include <cuda_bf16.h>
@@ -27,6 +32,8 @@ namespace skinny {
 namespace {
 
 constexpr int kHidden = 7168;
+constexpr uint64_t kExchangeLimitNs = 1000000000ull;  // 1 s for the CTA sums
+__device__ int g_reduce_err;  // nonzero: a cluster exchange wait ran out
 constexpr int kRowFrags = kHidden / 8;  // 896 fragments of 16 bytes
 constexpr int kMaxTP = 8;
 
@@ -78,9 +85,16 @@ __global__ void __launch_bounds__(ReduceShape<C>::kThreads)
     const int frag = rank * R::kFrags + tid;
     const size_t row_off = static_cast<size_t>(row) * kRowFrags + frag;
 
+    __shared__ alignas(8) unsigned long long recv_bar;  // the C CTA sums arrived
     if constexpr (C > 1) {
-        // Peers' shared memory is written below; make sure every CTA has started.
-        asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+        // Each CTA's sum goes to every peer with st.async, completing bytes on the
+        // peer's barrier; the barriers must be initialised (and published to the
+        // cluster) before any peer may send.
+        if (tid == 0) {
+            ptx::mbar_init(ptx::smem_addr(&recv_bar), 1);
+            ptx::fence_barrier_init();
+        }
+        asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
     }
 
     uint4 gw = make_uint4(0, 0, 0, 0);
@@ -194,17 +208,33 @@ __global__ void __launch_bounds__(ReduceShape<C>::kThreads)
     if ((tid & 31) == 0) warp_sums[tid >> 5] = ss;
     __syncthreads();
     if constexpr (C > 1) {
-        asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+        asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+        const uint32_t bar = ptx::smem_addr(&recv_bar);
         if (tid == 0) {
             float block = warp_sums[0];
 #pragma unroll
             for (int w = 1; w < R::kWarps; ++w) block = __fadd_rn(block, warp_sums[w]);
+            ptx::mbar_arrive_expect_tx(bar, C * 4);
             const uint32_t local = ptx::smem_addr(&parts[rank]);
 #pragma unroll
             for (int peer = 0; peer < C; ++peer)
-                ptx::st_cluster_f32(ptx::map_to_cluster_rank(local, peer), block);
+                asm volatile(
+                    "st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(
+                        ptx::map_to_cluster_rank(local, peer)),
+                    "r"(__float_as_uint(block)), "r"(ptx::map_to_cluster_rank(bar, peer))
+                    : "memory");
         }
-        ptx::cluster_sync();
+        // Every CTA's sum has landed here (bounded wait: a sum that never comes
+        // is recorded and the row's output is unspecified).
+        if (!ptx::mbar_try_wait(bar, 0)) {
+            const uint64_t t0 = ptx::global_timer_ns();
+            for (uint32_t spin = 1; !ptx::mbar_try_wait(bar, 0); ++spin) {
+                if ((spin & 15u) == 0 && ptx::global_timer_ns() - t0 > kExchangeLimitNs) {
+                    if (tid == 0) atomicOr(&g_reduce_err, 1);
+                    break;
+                }
+            }
+        }
     } else {
         if (tid == 0) {
             float block = warp_sums[0];
@@ -301,6 +331,13 @@ cudaError_t launch_reduce_rmsnorm_splitk(void *partials, int TP, const void *res
                                          cudaStream_t stream, bool pdl) {
     return launch_any<true>(partials, TP, residual, gamma, out, residual_out, M, eps,
                             ctas_per_row, stream, pdl, fix);
+}
+
+cudaError_t reduce_error_word(int *value, bool clear) {
+    cudaError_t e = cudaMemcpyFromSymbol(value, g_reduce_err, sizeof(int));
+    if (e != cudaSuccess || !clear || *value == 0) return e;
+    const int zero = 0;
+    return cudaMemcpyToSymbol(g_reduce_err, &zero, sizeof(int));
 }
 
 }  // namespace skinny
