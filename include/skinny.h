@@ -369,6 +369,21 @@ SKINNY_API int skinny_gemm_cta_pieces(int M, int N, int K, int num_sms, int cta,
 SKINNY_API int skinny_watchdog_selftest(const void *x, const void *W, void *out, int M, int N,
                              int K, long long timeout_ns, void *stream);
 
+/*
+ * skinny_reduce_selftest -- exercise reduce_residual_rmsnorm's bounded wait.
+ *   Checks its arguments as reduce_residual_rmsnorm does, then launches the
+ *   reduce with one 8-CTA cluster per row in which the last CTA keeps its
+ *   share of the row's sum of squares to itself: every CTA's wait for the
+ *   cluster's sums runs out after timeout_ns nanoseconds (1e3 <= timeout_ns <=
+ *   2e9), is recorded, and ends; out and residual_out are left unspecified.
+ *   skinny_device_error() then reports bit 128 and clears it. No state outlives
+ *   the call: the next reduce runs normally. For tests of the failure path
+ *   only.
+ */
+SKINNY_API int skinny_reduce_selftest(const void *partials, int TP, const void *residual,
+                                      const void *gamma, void *out, void *residual_out, int M,
+                                      float eps, long long timeout_ns, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -102,6 +102,8 @@ def load_library(path: str = LIBRARY):
     lib.skinny_gemm_cta_pieces.restype = i32
     lib.skinny_watchdog_selftest.argtypes = [vp, vp, vp, i32, i32, i32, ctypes.c_longlong, vp]
     lib.skinny_watchdog_selftest.restype = i32
+    lib.skinny_reduce_selftest.argtypes = [vp, i32, vp, vp, vp, vp, i32, f32, ctypes.c_longlong, vp]
+    lib.skinny_reduce_selftest.restype = i32
     _lib = lib
     return lib
 
@@ -307,3 +309,21 @@ def watchdog_selftest(x, W, out, timeout_ns, stream=None):
                                                  M, N, K, int(timeout_ns),
                                                  _stream_handle(stream))
     _check(st, "skinny_watchdog_selftest")
+
+
+def reduce_selftest(partials, residual, gamma, out, residual_out, eps, timeout_ns, stream=None):
+    """Launch the reduce with a cluster exchange that can never complete (see skinny.h)."""
+    _bf16_cuda(partials, "partials")
+    if partials.dim() != 3 or partials.shape[2] != HIDDEN:
+        raise ValueError(f"partials must be [TP, M, {HIDDEN}], got {tuple(partials.shape)}")
+    TP, M, _ = partials.shape
+    if residual is not None:
+        _bf16_cuda(residual, "residual", (M, HIDDEN))
+    _bf16_cuda(gamma, "gamma", (HIDDEN,))
+    _bf16_cuda(out, "out", (M, HIDDEN))
+    _bf16_cuda(residual_out, "residual_out", (M, HIDDEN))
+    st = load_library().skinny_reduce_selftest(
+        partials.data_ptr(), TP, residual.data_ptr() if residual is not None else None,
+        gamma.data_ptr(), out.data_ptr(), residual_out.data_ptr(), M, float(eps),
+        int(timeout_ns), _stream_handle(stream))
+    _check(st, "skinny_reduce_selftest")

@@ -391,6 +391,43 @@ int reduce_ctas_per_row(int M, int TP, bool residual) {
     return 8;
 }
 
+// The reduce's argument checks that need no device: pointers, shapes, eps,
+// alignment, aliasing.
+int reduce_arg_checks(const void *partials, int TP, const void *residual, const void *gamma,
+                      const void *out, const void *residual_out, int M, float eps) {
+    if (!partials || !gamma || !out || !residual_out) return SKINNY_ERR_NULL;
+    if (TP < 1 || TP > SKINNY_REDUCE_MAX_TP || M < 1 || M > SKINNY_REDUCE_MAX_M)
+        return SKINNY_ERR_SHAPE;
+    if (!(eps > 0.0f) || !std::isfinite(eps)) return SKINNY_ERR_ARG;
+    if (!aligned(partials, 16) || !aligned(gamma, 16) || !aligned(out, 16) ||
+        !aligned(residual_out, 16) || (residual && !aligned(residual, 16)))
+        return SKINNY_ERR_ALIGN;
+    const size_t row = static_cast<size_t>(M) * SKINNY_HIDDEN * 2;
+    const size_t pb = row * TP, gb = SKINNY_HIDDEN * 2;
+    if (overlaps(out, row, residual_out, row) || overlaps(out, row, partials, pb) ||
+        overlaps(out, row, gamma, gb) || overlaps(residual_out, row, partials, pb) ||
+        overlaps(residual_out, row, gamma, gb) || (residual && overlaps(out, row, residual, row)))
+        return SKINNY_ERR_ALIAS;
+    // residual_out may be residual itself (element-wise in-place), nothing else.
+    if (residual && residual != residual_out && overlaps(residual_out, row, residual, row))
+        return SKINNY_ERR_ALIAS;
+    return SKINNY_OK;
+}
+
+// The current device, and the reduce's pointers on it.
+int reduce_device_checks(const void *partials, const void *residual, const void *gamma,
+                         const void *out, const void *residual_out, int *dev) {
+    int st;
+    if ((st = current_device(dev))) return st;
+    DeviceState *d = nullptr;
+    if ((st = device_state(*dev, &d))) return st;
+    if ((st = check_device_pointer(partials, *dev)) || (st = check_device_pointer(gamma, *dev)) ||
+        (st = check_device_pointer(out, *dev)) || (st = check_device_pointer(residual_out, *dev)) ||
+        (residual && (st = check_device_pointer(residual, *dev))))
+        return st;
+    return SKINNY_OK;
+}
+
 }  // namespace
 }  // namespace skinny
 
@@ -526,35 +563,34 @@ int skinny_watchdog_selftest(const void *x, const void *W, void *out, int M, int
 int reduce_residual_rmsnorm_ex(const void *partials, int TP, const void *residual,
                                const void *gamma, void *out, void *residual_out, int M, float eps,
                                const skinny_launch_opts *opts, void *stream) {
-    if (!partials || !gamma || !out || !residual_out) return SKINNY_ERR_NULL;
-    if (TP < 1 || TP > SKINNY_REDUCE_MAX_TP || M < 1 || M > SKINNY_REDUCE_MAX_M)
-        return SKINNY_ERR_SHAPE;
-    if (!(eps > 0.0f) || !std::isfinite(eps)) return SKINNY_ERR_ARG;
-    if (!aligned(partials, 16) || !aligned(gamma, 16) || !aligned(out, 16) ||
-        !aligned(residual_out, 16) || (residual && !aligned(residual, 16)))
-        return SKINNY_ERR_ALIGN;
-    const size_t row = static_cast<size_t>(M) * SKINNY_HIDDEN * 2;
-    const size_t pb = row * TP, gb = SKINNY_HIDDEN * 2;
-    if (overlaps(out, row, residual_out, row) || overlaps(out, row, partials, pb) ||
-        overlaps(out, row, gamma, gb) || overlaps(residual_out, row, partials, pb) ||
-        overlaps(residual_out, row, gamma, gb) || (residual && overlaps(out, row, residual, row)))
-        return SKINNY_ERR_ALIAS;
-    // residual_out may be residual itself (element-wise in-place), nothing else.
-    if (residual && residual != residual_out && overlaps(residual_out, row, residual, row))
-        return SKINNY_ERR_ALIAS;
-    int dev, st;
     LaunchSettings ls;
-    if ((st = resolve_settings(opts, &ls))) return st;
-    if ((st = current_device(&dev))) return st;
-    DeviceState *d = nullptr;
-    if ((st = device_state(dev, &d))) return st;
-    if ((st = check_device_pointer(partials, dev)) || (st = check_device_pointer(gamma, dev)) ||
-        (st = check_device_pointer(out, dev)) || (st = check_device_pointer(residual_out, dev)) ||
-        (residual && (st = check_device_pointer(residual, dev))))
+    int dev, st;
+    if ((st = reduce_arg_checks(partials, TP, residual, gamma, out, residual_out, M, eps)) ||
+        (st = resolve_settings(opts, &ls)) ||
+        (st = reduce_device_checks(partials, residual, gamma, out, residual_out, &dev)))
         return st;
     cudaError_t e = launch_reduce_rmsnorm(partials, TP, residual, gamma, out, residual_out, M, eps,
                                           reduce_ctas_per_row(M, TP, residual != nullptr),
                                           static_cast<cudaStream_t>(stream), ls.pdl);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return SKINNY_ERR_LAUNCH;
+    }
+    return SKINNY_OK;
+}
+
+int skinny_reduce_selftest(const void *partials, int TP, const void *residual, const void *gamma,
+                           void *out, void *residual_out, int M, float eps, long long timeout_ns,
+                           void *stream) {
+    if (timeout_ns < 1000 || timeout_ns > 2000000000LL) return SKINNY_ERR_ARG;
+    int dev, st;
+    if ((st = reduce_arg_checks(partials, TP, residual, gamma, out, residual_out, M, eps)) ||
+        (st = reduce_device_checks(partials, residual, gamma, out, residual_out, &dev)))
+        return st;
+    cudaError_t e = launch_reduce_rmsnorm_selftest(partials, TP, residual, gamma, out,
+                                                   residual_out, M, eps,
+                                                   static_cast<unsigned long long>(timeout_ns),
+                                                   static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) {
         cudaGetLastError();
         return SKINNY_ERR_LAUNCH;

@@ -102,6 +102,15 @@ cudaError_t launch_reduce_rmsnorm_splitk(void *partials, int TP, const void *res
                                          float eps, int ctas_per_row, const SplitKPartials &fix,
                                          cudaStream_t stream, bool pdl);
 
+// The plain reduce with 8-CTA clusters whose last CTA keeps its sum of squares
+// to itself, every exchange wait limited to limit_ns: the failure-path
+// self-test (the waits run out, are recorded in the reduce's error word and
+// end; the outputs are unspecified).
+cudaError_t launch_reduce_rmsnorm_selftest(const void *partials, int TP, const void *residual,
+                                           const void *gamma, void *out, void *residual_out,
+                                           int M, float eps, unsigned long long limit_ns,
+                                           cudaStream_t stream);
+
 // The reduce kernel's own error word on the current device (nonzero: a
 // cluster exchange wait ran out), cleared after reading if `clear`.
 cudaError_t reduce_error_word(int *value, bool clear);

@@ -68,12 +68,15 @@ __device__ __forceinline__ uint4 pack8(const uint32_t (&b)[8]) {
 // partials ("drafter/linears": FP32 split-K partials, one BF16 rounding): the
 // partials of the fragment's 8 columns added in K order and rounded once, as the
 // GEMM's own finisher would; the result is also stored to slot 0.
-template <int C, bool RES, bool FIX>
+// TEST (the failure-path self-test only): the last CTA of each cluster keeps
+// its sum to itself, so that every wait of the cluster runs out, after limit_ns
+// instead of the regular limit.
+template <int C, bool RES, bool FIX, bool TEST = false>
 __global__ void __launch_bounds__(ReduceShape<C>::kThreads)
     reduce_rmsnorm_kernel(const uint4 *partials, int TP, const uint4 *residual,
                           const uint4 *__restrict__ gamma, uint4 *__restrict__ out,
                           uint4 *residual_out, int M, float eps, uint4 *slot0,
-                          SplitKPartials fix) {
+                          SplitKPartials fix, unsigned long long limit_ns) {
     using R = ReduceShape<C>;
     __shared__ float warp_sums[R::kWarps];
     __shared__ float parts[C];
@@ -218,7 +221,8 @@ __global__ void __launch_bounds__(ReduceShape<C>::kThreads)
             const uint32_t local = ptx::smem_addr(&parts[rank]);
 #pragma unroll
             for (int peer = 0; peer < C; ++peer)
-                asm volatile(
+                if (!TEST || rank != C - 1)
+                    asm volatile(
                     "st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(
                         ptx::map_to_cluster_rank(local, peer)),
                     "r"(__float_as_uint(block)), "r"(ptx::map_to_cluster_rank(bar, peer))
@@ -229,7 +233,8 @@ __global__ void __launch_bounds__(ReduceShape<C>::kThreads)
         if (!ptx::mbar_try_wait(bar, 0)) {
             const uint64_t t0 = ptx::global_timer_ns();
             for (uint32_t spin = 1; !ptx::mbar_try_wait(bar, 0); ++spin) {
-                if ((spin & 15u) == 0 && ptx::global_timer_ns() - t0 > kExchangeLimitNs) {
+                if ((spin & 15u) == 0 &&
+                    ptx::global_timer_ns() - t0 > (TEST ? limit_ns : kExchangeLimitNs)) {
                     if (tid == 0) atomicOr(&g_reduce_err, 1);
                     break;
                 }
@@ -258,10 +263,11 @@ __global__ void __launch_bounds__(ReduceShape<C>::kThreads)
     }
 }
 
-template <int C, bool RES, bool FIX>
+template <int C, bool RES, bool FIX, bool TEST = false>
 cudaError_t launch_c(const void *partials, int TP, const void *residual, const void *gamma,
                      void *out, void *residual_out, int M, float eps, cudaStream_t stream,
-                     bool pdl, const SplitKPartials &fix) {
+                     bool pdl, const SplitKPartials &fix,
+                     unsigned long long limit_ns = kExchangeLimitNs) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(C, M, 1);
     cfg.blockDim = dim3(ReduceShape<C>::kThreads, 1, 1);
@@ -283,12 +289,13 @@ cudaError_t launch_c(const void *partials, int TP, const void *residual, const v
     }
     cfg.attrs = attr;
     cfg.numAttrs = n;
-    return cudaLaunchKernelEx(&cfg, reduce_rmsnorm_kernel<C, RES, FIX>,
+    return cudaLaunchKernelEx(&cfg, reduce_rmsnorm_kernel<C, RES, FIX, TEST>,
                               static_cast<const uint4 *>(partials), TP,
                               static_cast<const uint4 *>(residual),
                               static_cast<const uint4 *>(gamma), static_cast<uint4 *>(out),
                               static_cast<uint4 *>(residual_out), M, eps,
-                              const_cast<uint4 *>(static_cast<const uint4 *>(partials)), fix);
+                              const_cast<uint4 *>(static_cast<const uint4 *>(partials)), fix,
+                              limit_ns);
 }
 
 template <int C, bool FIX>
@@ -331,6 +338,18 @@ cudaError_t launch_reduce_rmsnorm_splitk(void *partials, int TP, const void *res
                                          cudaStream_t stream, bool pdl) {
     return launch_any<true>(partials, TP, residual, gamma, out, residual_out, M, eps,
                             ctas_per_row, stream, pdl, fix);
+}
+
+cudaError_t launch_reduce_rmsnorm_selftest(const void *partials, int TP, const void *residual,
+                                           const void *gamma, void *out, void *residual_out,
+                                           int M, float eps, unsigned long long limit_ns,
+                                           cudaStream_t stream) {
+    const SplitKPartials none = {};
+    if (residual)
+        return launch_c<8, true, false, true>(partials, TP, residual, gamma, out, residual_out, M,
+                                              eps, stream, false, none, limit_ns);
+    return launch_c<8, false, false, true>(partials, TP, residual, gamma, out, residual_out, M,
+                                           eps, stream, false, none, limit_ns);
 }
 
 cudaError_t reduce_error_word(int *value, bool clear) {

@@ -387,6 +387,26 @@ def test_ex_entry_points_validate_options_before_cuda(lib):
                                    ctypes.byref(sk.LaunchOpts(1, 0)), None) == 2
 
 
+def test_selftests_check_their_limits_before_cuda(lib):
+    """Both failure-path self-tests reject a wait limit outside [1 us, 2 s] with
+    SKINNY_ERR_ARG before touching CUDA; the reduce's also checks its other
+    arguments as reduce_residual_rmsnorm does."""
+    import torch
+    buf = ctypes.create_string_buffer(1 << 22)
+    p = ctypes.addressof(buf) + (-ctypes.addressof(buf)) % 256
+    row = 7168 * 2
+    part, res, gam, out, rout = p, p + 8 * row * 2, p + 10 * row * 2, p + 11 * row * 2, \
+        p + 13 * row * 2
+    for bad in (0, 999, 3_000_000_000):
+        assert lib.skinny_watchdog_selftest(p, p + 4096, p + 65536, 4, 16, 64, bad, None) == 10
+        assert lib.skinny_reduce_selftest(part, 8, res, gam, out, rout, 2, 1e-6, bad, None) == 10
+    assert lib.skinny_reduce_selftest(part, 9, res, gam, out, rout, 2, 1e-6, 10**6, None) == 2
+    assert lib.skinny_reduce_selftest(None, 8, res, gam, out, rout, 2, 1e-6, 10**6, None) == 1
+    assert lib.skinny_reduce_selftest(part, 8, res, gam, out, out, 2, 1e-6, 10**6, None) == 6
+    if not torch.cuda.is_available():
+        assert lib.skinny_reduce_selftest(part, 8, res, gam, out, rout, 2, 1e-6, 10**6, None) == 4
+
+
 def test_process_settings_are_thread_safe_and_ex_calls_leave_them(lib):
     """Two host threads: one flips the process-wide settings, the other makes
     _ex calls with its own settings. The _ex calls never change the process-wide

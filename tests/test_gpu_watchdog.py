@@ -58,3 +58,48 @@ def test_selftest_rejects_out_of_range_limits(cuda_ok):
     for bad in (0, 999, 3_000_000_000):
         with pytest.raises(sk.SkinnyError):
             sk.watchdog_selftest(x, W, out, timeout_ns=bad)
+
+
+REDUCE_EXCHANGE_BIT = 128  # a reduce cluster's wait for its CTA sums ran out
+
+
+def test_reduce_exchange_wait_reports_and_recovers(cuda_ok):
+    """The reduce's bounded wait for its cluster's sums of squares: a cluster
+    whose last CTA never sends its sum ends every wait after the limit, the
+    host reads bit 128 once, and the next reduce returns the right bits."""
+    TP, M = 8, 16
+    inp = workloads.reduce_inputs(TP, M, workloads.seed_for("reduce watchdog", TP, M), True,
+                                  device=torch.device("cuda"))
+    out = torch.empty(M, workloads.HIDDEN, dtype=torch.bfloat16, device="cuda")
+    rout = torch.empty_like(out)
+    sk.reduce_residual_rmsnorm(inp.partials, inp.residual, inp.gamma, out, rout, 1e-6)
+    torch.cuda.synchronize()
+    ref, rref = out.clone(), rout.clone()
+    assert sk.device_error() == (0, 0)
+
+    junk, rjunk = torch.empty_like(out), torch.empty_like(rout)
+    sk.reduce_selftest(inp.partials, inp.residual, inp.gamma, junk, rjunk, 1e-6,
+                       timeout_ns=5_000_000)  # 5 ms limit
+    torch.cuda.synchronize()
+    status, word = sk.device_error()
+    assert status == 9, sk.status_string(status)
+    assert word == REDUCE_EXCHANGE_BIT
+    assert sk.device_error() == (0, 0)
+
+    out.zero_()
+    rout.zero_()
+    sk.reduce_residual_rmsnorm(inp.partials, inp.residual, inp.gamma, out, rout, 1e-6)
+    torch.cuda.synchronize()
+    assert sk.device_error() == (0, 0)
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    assert torch.equal(rout.view(torch.int16), rref.view(torch.int16))
+
+
+def test_reduce_selftest_rejects_out_of_range_limits(cuda_ok):
+    TP, M = 8, 1
+    inp = workloads.reduce_inputs(TP, M, 5, False, device=torch.device("cuda"))
+    out = torch.empty(M, workloads.HIDDEN, dtype=torch.bfloat16, device="cuda")
+    rout = torch.empty_like(out)
+    for bad in (0, 999, 3_000_000_000):
+        with pytest.raises(sk.SkinnyError):
+            sk.reduce_selftest(inp.partials, None, inp.gamma, out, rout, 1e-6, timeout_ns=bad)
