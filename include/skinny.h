@@ -93,6 +93,18 @@ typedef struct {
     int pdl;          /* 1: programmatic dependent launch (see skinny_set_pdl), 0: off */
     int l2_prefetch;  /* decode GEMM deep-ring L2 lead in [0, 64] (see
                          skinny_set_l2_prefetch); ignored by the reduce */
+    int l2_after_reduce;
+    /* decode GEMM only, for the call that follows decode_gemm_bf16_reduce_rmsnorm
+     * in the same stream (a layer chain's next first GEMM): weight blocks in
+     * [0, 64] each CTA prefetches into L2, beyond its ring's first fill, as soon
+     * as that call's reduce has seen its GEMM complete -- so that HBM streams
+     * this GEMM's weights while the reduce runs, without slowing the previous
+     * GEMM's last CTAs. The CTA waits at most 50 us for that signal, then goes
+     * on without it. 0 or SKINNY_OPT_DEFAULT: off. Timing only: no result bit
+     * depends on it. The signal is one word of the device's scratch, shared by
+     * every stream like the split-K scratch; it stays set until the next
+     * decode_gemm_bf16_reduce_rmsnorm's GEMM clears it, so a call that is not
+     * behind one may prefetch at once. */
 } skinny_launch_opts;
 
 /*

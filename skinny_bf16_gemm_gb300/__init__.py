@@ -35,17 +35,20 @@ class SkinnyError(RuntimeError):
 
 
 class LaunchOpts(ctypes.Structure):
-    """skinny_launch_opts: per-call settings, -1 = the process-wide one."""
-    _fields_ = [("pdl", ctypes.c_int), ("l2_prefetch", ctypes.c_int)]
+    """skinny_launch_opts: per-call settings, -1 = the process-wide one (for
+    l2_after_reduce: off)."""
+    _fields_ = [("pdl", ctypes.c_int), ("l2_prefetch", ctypes.c_int),
+                ("l2_after_reduce", ctypes.c_int)]
 
 
-def _opts(pdl, l2_prefetch):
-    """A LaunchOpts for the given keywords, or None if both are None (the call
+def _opts(pdl, l2_prefetch, l2_after_reduce=None):
+    """A LaunchOpts for the given keywords, or None if all are None (the call
     then goes to the plain entry point and the process-wide settings)."""
-    if pdl is None and l2_prefetch is None:
+    if pdl is None and l2_prefetch is None and l2_after_reduce is None:
         return None
     return LaunchOpts(-1 if pdl is None else int(bool(pdl)),
-                      -1 if l2_prefetch is None else int(l2_prefetch))
+                      -1 if l2_prefetch is None else int(l2_prefetch),
+                      -1 if l2_after_reduce is None else int(l2_after_reduce))
 
 
 class GemmPlan(ctypes.Structure):
@@ -136,12 +139,13 @@ def _bf16_cuda(t, name, shape=None):
         raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
 
 
-def decode_gemm_bf16(x, W, out, stream=None, pdl=None, l2_prefetch=None):
+def decode_gemm_bf16(x, W, out, stream=None, pdl=None, l2_prefetch=None, l2_after_reduce=None):
     """out[M, N] = x[M, K] @ W[N, K]^T on the current (or given) stream.
 
     x, W, out: contiguous CUDA bfloat16 tensors. Returns ``out``. pdl and
     l2_prefetch, when given, are this call's launch settings (decode_gemm_bf16_ex)
-    instead of the process-wide ones.
+    instead of the process-wide ones; l2_after_reduce (weight blocks, 0..64) is
+    for a call right behind decode_gemm_bf16_reduce_rmsnorm (see skinny.h).
     """
     _bf16_cuda(x, "x")
     _bf16_cuda(W, "W")
@@ -150,7 +154,7 @@ def decode_gemm_bf16(x, W, out, stream=None, pdl=None, l2_prefetch=None):
     M, K = x.shape
     N = W.shape[0]
     _bf16_cuda(out, "out", (M, N))
-    o = _opts(pdl, l2_prefetch)
+    o = _opts(pdl, l2_prefetch, l2_after_reduce)
     lib = load_library()
     if o is None:
         st = lib.decode_gemm_bf16(x.data_ptr(), W.data_ptr(), out.data_ptr(), M, N, K,

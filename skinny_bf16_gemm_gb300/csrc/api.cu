@@ -29,6 +29,9 @@ struct DeviceState {
     unsigned *flags = nullptr;
     int *err = nullptr;
     size_t flag_bytes = 0;
+    // decode_gemm_bf16_reduce_rmsnorm's "its GEMM is complete" word (in the
+    // scratch's last 256 bytes, after the error word).
+    unsigned *gemm_done = nullptr;
     // A host-mapped word the decode GEMM sets when one of its waits runs out:
     // the host reads it without synchronising, so the next call can refuse to
     // run on scratch a kernel left half used (host_err) -- and the kernel's
@@ -125,6 +128,7 @@ int ensure_scratch(int dev, cudaStream_t stream, DeviceState **out) {
         d->flags = reinterpret_cast<unsigned *>(static_cast<char *>(p) + partial_bytes);
         d->err = reinterpret_cast<int *>(static_cast<char *>(p) + partial_bytes + flag_bytes);
         d->flag_bytes = flag_bytes;
+        d->gemm_done = reinterpret_cast<unsigned *>(d->err) + 32;
     }
     *out = d;
     return SKINNY_OK;
@@ -206,6 +210,7 @@ int pending_timeout(const DeviceState *d) {
 struct LaunchSettings {
     bool pdl;
     int l2_lead;
+    int l2_after_reduce;
 };
 
 int resolve_settings(const skinny_launch_opts *opts, LaunchSettings *out) {
@@ -213,13 +218,17 @@ int resolve_settings(const skinny_launch_opts *opts, LaunchSettings *out) {
         if (opts->pdl < SKINNY_OPT_DEFAULT || opts->pdl > 1) return SKINNY_ERR_ARG;
         if (opts->l2_prefetch < SKINNY_OPT_DEFAULT || opts->l2_prefetch > kL2LeadMax)
             return SKINNY_ERR_ARG;
+        if (opts->l2_after_reduce < SKINNY_OPT_DEFAULT || opts->l2_after_reduce > kL2LeadMax)
+            return SKINNY_ERR_ARG;
     }
     std::lock_guard<std::mutex> lock(g_mutex);
     out->pdl = g_pdl;
     out->l2_lead = g_l2_lead;
+    out->l2_after_reduce = 0;
     if (opts != nullptr) {
         if (opts->pdl != SKINNY_OPT_DEFAULT) out->pdl = opts->pdl != 0;
         if (opts->l2_prefetch != SKINNY_OPT_DEFAULT) out->l2_lead = opts->l2_prefetch;
+        if (opts->l2_after_reduce > 0) out->l2_after_reduce = opts->l2_after_reduce;
     }
     return SKINNY_OK;
 }
@@ -269,6 +278,8 @@ int gemm_launch(const void *x, const void *W, void *out, int M, int N, int K, vo
     a.scale = scale;
     const bool pdl = ls.pdl;
     a.l2_lead = ls.l2_lead;
+    a.gemm_done = d->gemm_done;
+    a.l2_after_reduce = ls.l2_after_reduce;
     // Split tiles of 64-row accumulators, every CTA within at most two tiles (two
     // scratch slots), plain output: the GEMM only publishes its partials and a
     // small kernel finishes them (same order, same bits). A finisher CTA would
@@ -514,6 +525,8 @@ int decode_gemm_bf16_reduce_rmsnorm_ex(const void *x, const void *W, void *parti
     a.scale = 1.0f;
     a.publish_only = 1;
     a.l2_lead = l2_lead;
+    a.gemm_done = d->gemm_done;
+    a.clear_gemm_done = 1;
     if (launch_decode_gemm(w_map, x_map, a, mma_n, g.ctas, s, pdl, use_shallow_ring(g, pdl), dev) !=
         cudaSuccess) {
         cudaGetLastError();
@@ -522,6 +535,7 @@ int decode_gemm_bf16_reduce_rmsnorm_ex(const void *x, const void *W, void *parti
     SplitKPartials fix = {};
     fix.partials = d->partials;
     fix.slot_floats = kSlotFloats;
+    fix.gemm_done = d->gemm_done;
     fix.M = M;
     fix.N = N;
     fix.K = K;

@@ -54,6 +54,9 @@ constexpr uint64_t kDrainLimitNs = 200000000ull;  // 0.2 s for copies already is
 // beat 26 (most of a short range) by up to 1.4 us at N = 4096 and 3.5 us at
 // N = 6144-7168 (K = 7168, 0.4-0.7 MB per CTA); 0-4 are slower again.
 constexpr int kL2PrefetchShallow = 8;
+// The longest a producer waits for the previous GEMM's completion signal before
+// it goes on without the prefetch that depends on it (GemmArgs::l2_after_reduce).
+constexpr uint64_t kAfterReduceWaitNs = 50000ull;
 constexpr int kMaxShallowStages = 6;  // shallow rings have 5..6 stages, deep ones 9..11
 
 // MP: padded row count (MMA N). STAGES: shared-memory ring depth. The deep ring
@@ -247,6 +250,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tma_prefetch_l2_2d(&w_map, pf.kb * kBlockK, pf.t * kBlockN);
                 pf.next(g.kblocks);
             }
+            if (args.l2_after_reduce > 0) {
+                // Behind a reduce whose GEMM is complete, HBM would idle until this
+                // kernel's wait returns: prefetch more now. Not earlier, where the
+                // requests would slow that GEMM's last CTAs.
+                const uint64_t t0 = ptx::global_timer_ns();
+                bool go = ptx::ld_acquire_gpu(args.gemm_done) != 0u;
+                while (!go && ptx::global_timer_ns() - t0 < kAfterReduceWaitNs) {
+                    __nanosleep(128);
+                    go = ptx::ld_acquire_gpu(args.gemm_done) != 0u;
+                }
+                if (go) {
+                    const int rest = total - npre - npf;
+                    const int more = rest < args.l2_after_reduce ? rest : args.l2_after_reduce;
+                    for (int j = 0; j < more; ++j) {
+                        ptx::tma_prefetch_l2_2d(&w_map, pf.kb * kBlockK, pf.t * kBlockN);
+                        pf.next(g.kblocks);
+                    }
+                }
+            }
             ptx::pdl_wait();  // x may be the predecessor's output
             BlockCursor xc = start;
             for (int j = 0; j < npre; ++j) {
@@ -334,6 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ---------------- epilogue (128 threads) ----------------
         ptx::pdl_wait();  // scratch and out may still be in use by the predecessor
+        if (args.clear_gemm_done && blockIdx.x == 0 && threadIdx.x == 64) atomicExch(args.gemm_done, 0u);
         const int quarter = warp & 3;              // TMEM lanes 32*quarter .. +31
         const int row = quarter * 32 + lane;       // weight row within the tile
         const int etid = threadIdx.x - 64;

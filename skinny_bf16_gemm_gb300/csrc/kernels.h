@@ -40,6 +40,13 @@ struct GemmArgs {
     // Deep ring only: weight blocks each CTA prefetches into L2, beyond its ring's
     // first fill, before waiting on the previous kernel (skinny_set_l2_prefetch).
     int l2_lead;
+    // The "GEMM before the reduce is complete" word of decode_gemm_bf16_reduce_rmsnorm
+    // (set by its reduce, cleared by its GEMM), or nullptr. With l2_after_reduce > 0
+    // the producer waits (bounded) for it to be set and then prefetches that many
+    // more weight blocks into L2 before waiting on the previous kernel.
+    unsigned *gemm_done;
+    int l2_after_reduce;
+    int clear_gemm_done;  // 1: clear the word once the previous kernel is complete
 };
 
 // Default and largest l2_lead. Measured on GB300: 6 suits back-to-back GEMMs
@@ -55,6 +62,7 @@ struct SplitKPartials {
     const float *partials;  // [2 * ctas][slot_floats]
     int slot_floats;
     int M, N, K, ctas;
+    unsigned *gemm_done;    // set to 1 once the GEMM is complete (or nullptr)
 };
 
 // Pipeline depth and shared memory of the decode GEMM for a padded row count,

@@ -127,6 +127,12 @@ __global__ void __launch_bounds__(ReduceShape<C>::kThreads)
     }
     ptx::pdl_launch_dependents();
     ptx::pdl_wait();  // the partial rows may be the previous kernel's output
+    if constexpr (FIX) {
+        // The GEMM is complete: a decode GEMM waiting behind this kernel may
+        // prefetch its weights now (GemmArgs::l2_after_reduce).
+        if (fix.gemm_done != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && tid == 0)
+            atomicExch(fix.gemm_done, 1u);
+    }
 
     float h[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     float ss = 0.0f;

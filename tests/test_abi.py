@@ -367,7 +367,7 @@ def test_ex_entry_points_validate_options_before_cuda(lib):
     buf = ctypes.create_string_buffer(1 << 22)
     p = ctypes.addressof(buf) + (-ctypes.addressof(buf)) % 256
     bad = [sk.LaunchOpts(2, 0), sk.LaunchOpts(-2, 0), sk.LaunchOpts(1, 65),
-           sk.LaunchOpts(0, -2)]
+           sk.LaunchOpts(0, -2), sk.LaunchOpts(1, 0, 65), sk.LaunchOpts(1, 0, -2)]
     row = 7168 * 2
     part, res, gam, out, rout = p, p + 8 * row * 2, p + 10 * row * 2, p + 11 * row * 2, \
         p + 13 * row * 2

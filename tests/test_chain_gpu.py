@@ -97,14 +97,15 @@ def test_chain_eager_and_graph_replay_give_the_same_bits(chain_inputs):
 def test_fused_chain_equals_unfused_chain(chain_inputs):
     """The chain with decode_gemm_bf16_reduce_rmsnorm for each layer's second GEMM
     and reduce gives the unfused chain's rows bit for bit, with or without PDL,
-    whatever the decode GEMM's L2 lead; the chain's per-call settings leave the
-    process-wide ones as the caller set them."""
+    whatever the decode GEMM's L2 lead and its prefetch after the reduce; the
+    chain's per-call settings leave the process-wide ones as the caller set them."""
     inp = chain_inputs
     rows = []
-    for fused, lead, pdl in ((False, 6, True), (True, 0, True), (True, 6, False),
-                             (False, 0, False), (True, 0, False)):
+    for fused, lead, pdl, after in ((False, 6, True, 16), (True, 0, True, 16),
+                                    (True, 0, True, 0), (True, 6, False, 64),
+                                    (False, 0, False, 16), (True, 0, False, 16)):
         chain = LayerChain(inp.W1, inp.W2, inp.peers, inp.gamma, CFG.M, CFG.eps, fused=fused,
-                           l2_prefetch=lead, pdl=pdl)
+                           l2_prefetch=lead, pdl=pdl, l2_after_reduce=after)
         chain.x.copy_(inp.x0)
         chain.res_in.copy_(inp.residual0)
         prev = sk.set_pdl(not pdl)

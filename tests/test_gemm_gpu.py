@@ -223,3 +223,26 @@ def test_gemm_l2_lead_changes_no_bits(cuda_ok, M, N, K):
         sk.set_l2_prefetch(prev_lead)
         sk.set_pdl(prev_pdl)
     check_gemm_sampled(x, W, base, sample_columns(N, count=256, seed=M))
+
+
+@pytest.mark.parametrize("M,N,K", [(16, 18432, 7168), (4, 2048, 7168)])
+def test_gemm_prefetch_after_reduce_changes_no_bits(cuda_ok, M, N, K):
+    """l2_after_reduce only moves weight prefetches in time: right behind
+    decode_gemm_bf16_reduce_rmsnorm (the reduce sets the word) and on its own
+    (the word as an earlier call left it), the bits are those of the plain call."""
+    x, W = gemm_inputs_device(M, N, K, workloads.seed_for("after reduce", M, N, K))
+    ref = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    sk.decode_gemm_bf16(x, W, ref)
+    inp = workloads.reduce_inputs(8, 16, 11, True, device=torch.device("cuda"))
+    x2, W2 = gemm_inputs_device(16, workloads.HIDDEN, 1024, 12)
+    out = torch.empty(16, workloads.HIDDEN, dtype=torch.bfloat16, device="cuda")
+    rout = torch.empty_like(out)
+    for behind_reduce in (True, False, True):
+        if behind_reduce:
+            sk.decode_gemm_bf16_reduce_rmsnorm(x2, W2, inp.partials, inp.residual, inp.gamma, out,
+                                               rout, 1e-6, pdl=True)
+        got = torch.full_like(ref, 5.0)
+        sk.decode_gemm_bf16(x, W, got, pdl=True, l2_prefetch=0, l2_after_reduce=16)
+        torch.cuda.synchronize()
+        assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
+    assert sk.device_error() == (0, 0)
