@@ -53,6 +53,9 @@ def parse():
     ap.add_argument("--l2-prefetch", type=int, default=0,
                     help="weight blocks each decode GEMM CTA (deep ring) prefetches to L2 "
                          "before its PDL wait, in the chain (library default 6)")
+    ap.add_argument("--l2-after-reduce", type=int, default=16,
+                    help="with --fused 1: weight blocks each first GEMM's CTA prefetches to L2 "
+                         "once the reduce before it has seen its GEMM complete (0: off)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true",
                     help="per-config GB/s of every GEMM and reduce config instead of the chain")
@@ -681,7 +684,7 @@ def main():
     inp = workloads.chain_inputs(cfg, replica_seed(workloads.seed_for("chain"), rank), device=device)
     chain = LayerChain(inp.W1, inp.W2, inp.peers, inp.gamma, cfg.M, cfg.eps, device=device,
                        fused=bool(args.fused), l2_prefetch=args.l2_prefetch,
-                       pdl=bool(args.pdl))
+                       pdl=bool(args.pdl), l2_after_reduce=args.l2_after_reduce)
     chain.x.copy_(inp.x0)
     chain.res_in.copy_(inp.residual0)
     sk.set_pdl(bool(args.pdl))
@@ -815,7 +818,8 @@ def main():
     e2e_steps = max(G, min(args.steps, 500)) // G * G
     chains = [chain] + [LayerChain(inp.W1, inp.W2, inp.peers, inp.gamma, cfg.M, cfg.eps,
                                    device=device, fused=bool(args.fused),
-                                   l2_prefetch=args.l2_prefetch, pdl=bool(args.pdl))
+                                   l2_prefetch=args.l2_prefetch, pdl=bool(args.pdl),
+                                   l2_after_reduce=args.l2_after_reduce)
                         for _ in range(2 * G - 1)]
     copy_stream = torch.cuda.Stream()
     inputs_ready = [torch.cuda.Event() for _ in range(2)]
@@ -877,6 +881,8 @@ def main():
         "config": workload_config(cfg, {"pdl": bool(args.pdl), "graph": bool(args.graph),
                                         "fused_gemm_reduce": bool(args.fused),
                                         "l2_prefetch_blocks": args.l2_prefetch,
+                                        "l2_after_reduce_blocks":
+                                            args.l2_after_reduce if args.fused else 0,
                                         "parallelism": "replicas" if world > 1 else "single"}),
         "hbm_frac_of_measured": value / peak,
         "hbm_frac_of_nominal_8000": value / 8000.0,
