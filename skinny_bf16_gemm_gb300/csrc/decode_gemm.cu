@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t bar_never = bar_drain + 8;
     const uint32_t bar_fix = bar_never + 8;             // split-K fix-up bulk copies
     volatile uint32_t *misc = reinterpret_cast<volatile uint32_t *>(smem + L::kMiscOffset);
-    // misc[0]: tensor-memory base, misc[1]: abort flag, misc[2]: "last to arrive" flag
+    // misc[0]: tensor-memory base, misc[1]: abort flag
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
@@ -182,7 +182,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_init(bar_never, 1);
         ptx::mbar_init(bar_fix, 1);
         misc[1] = 0u;
-        misc[2] = 0u;
         ptx::fence_barrier_init();
     }
     if (warp == 0) {
