@@ -141,6 +141,37 @@ __device__ __forceinline__ float output_value(float v, const GemmArgs &a) {
     return __fmul_rn(v, a.scale);
 }
 
+// Store rows 0..M-1 of one tile's output (this thread's column n = tile * 128 +
+// row; v[m] the values to round) through the idle ring: each thread puts its
+// BF16 values in shared memory, then the 128 epilogue threads write 16-byte
+// pieces of whole rows instead of one 2-byte store per row and thread. Needs
+// 16-byte aligned rows (N a multiple of 8) and a ring nothing uses any more.
+// Measured on GB300 for whole tiles of 32 and 64 padded rows with the deep
+// ring: 0.3-0.6 us faster per call at N = 18432; no gain for 16 rows or on
+// split tiles, and 0.2 us slower with the shallow ring, so only there.
+template <int MP>
+__device__ __forceinline__ void store_tile_staged(const float (&v)[MP], uint16_t *out, int M, int N,
+                                                  int tile, int row, int etid, uint32_t stage) {
+#pragma unroll
+    for (int m = 0; m < MP; ++m)
+        if (m < M)
+            asm volatile("st.shared.u16 [%0], %1;" ::"r"(stage + (m * kBlockN + row) * 2),
+                         "h"(to_bf16_bits(v[m])) : "memory");
+    ptx::named_barrier_sync(1, kEpilogueThreads);
+    const int pieces = M * (kBlockN / 8);
+    for (int i = etid; i < pieces; i += kEpilogueThreads) {
+        const int m = i / (kBlockN / 8), c = i % (kBlockN / 8);
+        const int n0 = tile * kBlockN + c * 8;
+        if (n0 < N) {
+            uint4 w;
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
+                         : "r"(stage + (m * kBlockN + c * 8) * 2) : "memory");
+            *reinterpret_cast<uint4 *>(out + static_cast<size_t>(m) * N + n0) = w;
+        }
+    }
+}
+
 template <int MP, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_gemm_kernel(const __grid_constant__ CUtensorMap w_map,
@@ -364,6 +395,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float *staging = reinterpret_cast<const float *>(smem);
         uint32_t fix_phase = 0;
         bool fix_pending = false;
+        // Whole tiles of 32 or 64 padded rows, deep ring, 16-byte aligned output
+        // rows: the last piece's tile goes out through the ring.
+        constexpr bool kStagedOut = MP >= 32 && STAGES > kMaxShallowStages;
+        const bool staged = kStagedOut && (reinterpret_cast<uintptr_t>(args.out) & 15) == 0 &&
+                            (g.N & 7) == 0;
 
         // Finish split tile t. This CTA holds the tile's first K blocks, so the
         // tile is its last piece: its own partial is in registers and the ring
@@ -469,6 +505,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int n = p.tile * kBlockN + row;
             if (p.kb0 == 0 && p.kb1 == g.kblocks && !args.publish_only) {
                 // Whole tile in this CTA: round once and store.
+                if (kStagedOut && staged && q == pieces - 1) {
+#pragma unroll
+                    for (int m = 0; m < MP; ++m) acc[m] = output_value(acc[m], args);
+                    store_tile_staged<MP>(acc, args.out, g.M, g.N, p.tile, row, etid, sbase);
+                    continue;
+                }
                 if (n < g.N) {
 #pragma unroll
                     for (int m = 0; m < MP; ++m)

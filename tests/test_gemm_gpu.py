@@ -246,3 +246,24 @@ def test_gemm_prefetch_after_reduce_changes_no_bits(cuda_ok, M, N, K):
         torch.cuda.synchronize()
         assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
     assert sk.device_error() == (0, 0)
+
+
+@pytest.mark.parametrize("M,N,K,offset", [(64, 18424, 7168, 0), (40, 18430, 7168, 0),
+                                          (33, 18432, 7168, 1), (64, 18432, 1024, 0)])
+def test_gemm_wide_whole_tiles_every_element(cuda_ok, M, N, K, offset):
+    """Whole tiles of 32 and 64 padded rows leave through the ring as 16-byte
+    row pieces when the output rows are 16-byte aligned: a ragged last tile
+    (N = 18424), rows a multiple of 2 bytes but not of 16 (N = 18430, and an
+    output starting one element into its buffer) take the element stores. Every
+    element against the oracle, and the same bits as the element stores give
+    (an unaligned copy of the output is written the other way)."""
+    x, W = gemm_inputs_device(M, N, K, workloads.seed_for("wide whole", M, N, K))
+    buf = torch.empty(M * N + offset, dtype=torch.bfloat16, device="cuda")
+    out = buf[offset:].view(M, N)
+    sk.decode_gemm_bf16(x, W, out)
+    torch.cuda.synchronize()
+    check_gemm_full(x, W, out)
+    other = torch.empty(M * N + 1, dtype=torch.bfloat16, device="cuda")[1:].view(M, N)
+    sk.decode_gemm_bf16(x, W, other)
+    torch.cuda.synchronize()
+    assert torch.equal(other.view(torch.int16), out.view(torch.int16))
