@@ -56,6 +56,9 @@ def parse():
     ap.add_argument("--l2-after-reduce", type=int, default=16,
                     help="with --fused 1: weight blocks each first GEMM's CTA prefetches to L2 "
                          "once the reduce before it has seen its GEMM complete (0: off)")
+    ap.add_argument("--e2e-group", type=int, default=4,
+                    help="end-to-end timing: steps per group of buffer sets whose inputs go up "
+                         "together (one cross-stream wait per group)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true",
                     help="per-config GB/s of every GEMM and reduce config instead of the chain")
@@ -806,7 +809,7 @@ def main():
     # group is done. Every step copies its own inputs in and its rows out inside
     # the timed region; one event per group (not per step) keeps the compute
     # stream's kernels chained under programmatic dependent launch.
-    G = 4
+    G = max(1, args.e2e_group)
     pin = dict(pin_memory=True)
     host_x = inp.x0.cpu().pin_memory()
     host_res = inp.residual0.cpu().pin_memory()
