@@ -47,13 +47,15 @@ def test_gemm_small_full_compare(cuda_ok, M, N, K):
 
 @pytest.mark.parametrize("M,N,K", [(32, 2048, 7168), (7, 1152, 18432), (1, 640, 7168),
                                    (64, 1024, 14336), (16, 18432, 7168), (8, 20480, 7168),
-                                   (16, 7168, 18432)])
+                                   (16, 7168, 18432), (64, 20480, 7168), (40, 18432, 7168)])
 def test_gemm_integer_inputs_bit_exact(cuda_ok, M, N, K):
     """x, W in [-4, 4]: all partial sums are integers below 2^24, so any FP32
     order is exact and the GPU must equal the oracle bit for bit. Pins the tile,
     split-K and transpose wiring independently of rounding: N = 18432 takes one
     whole tile per CTA (no split), N = 20480 more tiles than CTAs (whole tiles
-    between split ends), N = 7168 at K = 18432 the chain's stream-K split."""
+    between split ends; with 64 rows the in-kernel finisher's 32 KB partials),
+    N = 7168 at K = 18432 the chain's stream-K split, 40 rows at N = 18432 the
+    whole tiles stored through the ring."""
     x, W = gemm_inputs_device(M, N, K, workloads.seed_for("int", M, N, K), kind="int")
     out = run_gemm(x, W)
     check_gemm_full(x, W, out, exact_bits_required=True)
@@ -77,7 +79,7 @@ FULL_SIZE = ([(m, n, 7168) for m in (1, 2, 4, 8, 16, 24, 32) for n in (4096, 122
 # (N = 18432 on a GB300: 144 tiles for 152 SMs, no split-K), the chain's
 # stream-K GEMM (16 x 18432 -> 7168) and the largest lm_head shape.
 FULL_ELEMENT = [(1, 18432, 7168), (16, 18432, 7168), (32, 18432, 7168), (48, 18432, 7168),
-                (16, 7168, 18432), (32, 20480, 7168)]
+                (16, 7168, 18432), (32, 20480, 7168), (64, 20480, 7168)]
 
 
 @pytest.mark.parametrize("M,N,K", FULL_ELEMENT)
