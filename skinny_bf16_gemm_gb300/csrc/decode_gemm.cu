@@ -10,8 +10,9 @@
 //               (x rows padded to 16, 32 or 64; the padding rows are TMA zero
 //               fill), accumulating in tensor memory (two accumulator buffers);
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator (TMEM lane = weight row =
-//               output column n, column = output row m), one BF16 rounding, or
-//               the split-K fix-up.
+//               output column n, column = output row m), one BF16 rounding and
+//               the store (for whole tiles of 32/64 padded rows through the
+//               idle ring, as 16-byte row pieces), or the split-K fix-up.
 // Work split (plan.cuh): one whole 128-row tile per CTA when the tiles nearly fill
 // the GPU, otherwise the ceil(N/128) x ceil(K/64) weight blocks dealt to one CTA
 // per SM as equal contiguous ranges (stream-K). A tile whose K range is shared
@@ -24,8 +25,9 @@
 // long streams; the shallow ring for short ones under programmatic dependent
 // launch, so that the next kernel's CTA shares the SM. Before waiting on the
 // previous kernel in the stream the producer already streams the first STAGES
-// weight tiles and prefetches more into L2: weights never depend on the previous
-// kernel, x may.
+// weight tiles and prefetches more into L2 -- behind decode_gemm_bf16_reduce_rmsnorm
+// optionally more again once that call's reduce has seen its GEMM complete:
+// weights never depend on the previous kernel, x may.
 // Every wait is bounded (wait_limit_ns); a role that gives up records a bit in
 // the device error word, the CTA drains its in-flight copies and MMAs, frees its
 // tensor memory and exits.
