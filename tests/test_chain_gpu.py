@@ -75,11 +75,15 @@ def test_chain_step_with_pdl_matches_oracle_stage_by_stage(chain_inputs):
         x, res = outs[l], ress[l]
 
 
-def test_chain_eager_and_graph_replay_give_the_same_bits(chain_inputs):
+@pytest.mark.parametrize("fused", [False, True])
+def test_chain_eager_and_graph_replay_give_the_same_bits(chain_inputs, fused):
     """LayerChain (the benchmark's driver): an eager step with PDL, a second eager
-    step and a CUDA-graph replay of the step all produce identical rows."""
+    step and a CUDA-graph replay of the step all produce identical rows -- also
+    fused, where each first GEMM waits (bounded) for the reduce's signal and
+    prefetches after it, inside the graph too."""
     inp = chain_inputs
-    chain = LayerChain(inp.W1, inp.W2, inp.peers, inp.gamma, CFG.M, CFG.eps, pdl=True)
+    chain = LayerChain(inp.W1, inp.W2, inp.peers, inp.gamma, CFG.M, CFG.eps, pdl=True,
+                       fused=fused)
     chain.x.copy_(inp.x0)
     chain.res_in.copy_(inp.residual0)
     a_out, a_res = (t.clone() for t in chain.run())

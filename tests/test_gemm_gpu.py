@@ -251,7 +251,8 @@ def test_gemm_prefetch_after_reduce_changes_no_bits(cuda_ok, M, N, K):
 
 
 @pytest.mark.parametrize("M,N,K,offset", [(64, 18424, 7168, 0), (40, 18430, 7168, 0),
-                                          (33, 18432, 7168, 1), (64, 18432, 1024, 0)])
+                                          (33, 18432, 7168, 1), (64, 18432, 1024, 0),
+                                          (36, 18432, 1000, 0)])
 def test_gemm_wide_whole_tiles_every_element(cuda_ok, M, N, K, offset):
     """Whole tiles of 32 and 64 padded rows leave through the ring as 16-byte
     row pieces when the output rows are 16-byte aligned: a ragged last tile
