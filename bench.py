@@ -124,6 +124,19 @@ def recorded_traffic(shape_key):
     return None if entry is None else float(entry)
 
 
+def keep_streaming(device, seconds):
+    """Device-to-device copies of a 256 MB buffer for about `seconds` (host
+    time): keeps HBM and the SMs busy while the host waits on something."""
+    src = torch.empty(1 << 28, dtype=torch.uint8, device=device)
+    dst = torch.empty_like(src)
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        for _ in range(50):
+            dst.copy_(src)
+        torch.cuda.synchronize()
+    del src, dst
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle sampling during the timed region."""
 
@@ -701,6 +714,13 @@ def main():
     def step():
         return chain.replay() if chain.graph is not None else chain.run()
 
+    # The clock sampler needs a moment to start; the GPU streams plain device
+    # copies meanwhile (not chain steps) instead of idling, so that the warm-up
+    # and timed steps do not begin on a GPU coming out of an idle spell.
+    clocks = ClockSampler(local)
+    clocks.start()
+    keep_streaming(device, 0.3)
+
     # Warm-up (eager), then optionally capture the step as one graph.
     for _ in range(max(args.warmup, 3)):
         chain.run()
@@ -715,9 +735,6 @@ def main():
         raise RuntimeError(f"device error word {word} during warm-up")
 
     # ---- timed region: K steps, inputs resident ----
-    clocks = ClockSampler(local)
-    clocks.start()
-    time.sleep(0.3)
     barrier()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -818,7 +835,9 @@ def main():
     host_res_out = [torch.empty(cfg.M, cfg.hidden, dtype=torch.bfloat16, **pin) for _ in range(2 * G)]
     h2d = (host_x.numel() + host_res.numel() + sum(p.numel() for p in host_peers)) * 2
     d2h = (host_out[0].numel() + host_res_out[0].numel()) * 2
-    e2e_steps = max(G, min(args.steps, 500)) // G * G
+    # At least 200 steps (at most 500): the copy pipeline's fill and drain are a
+    # few steps' worth, so a short run would mostly time those.
+    e2e_steps = max(200, min(args.steps, 500)) // G * G
     chains = [chain] + [LayerChain(inp.W1, inp.W2, inp.peers, inp.gamma, cfg.M, cfg.eps,
                                    device=device, fused=bool(args.fused),
                                    l2_prefetch=args.l2_prefetch, pdl=bool(args.pdl),
@@ -903,7 +922,7 @@ def main():
                     "reduce_gbs": cfg.reduce().algorithmic_bytes() / (reduce_ms * 1e-3) / 1e9},
         "clocks": clock_info,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": e2e_steps},
         "gpu_launches": args.steps * chain.launches_per_step(),
     }
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
