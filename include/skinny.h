@@ -29,7 +29,10 @@
  *    from then on every call that uses the decode GEMM's scratch on that device
  *    returns SKINNY_ERR_TIMEOUT without launching, until skinny_device_error()
  *    reads and clears the error (and re-arms the scratch). The output of the
- *    kernel that gave up is unspecified.
+ *    kernel that gave up is unspecified. The reduce kernel's wait for its
+ *    cluster's sums of squares is bounded too (1 s); one that runs out leaves
+ *    that call's output unspecified and is reported by skinny_device_error()
+ *    (bit 128), without holding back later calls (the reduce keeps no state).
  *  - Nothing is allocated per call. decode_gemm_bf16 uses a per-device scratch
  *    area (split-K partial sums, published-partial flags, an error word, plus
  *    one page of host-mapped memory) that its first call on each device
@@ -40,7 +43,9 @@
  *  - Launch settings: programmatic dependent launch and the decode GEMM's L2
  *    lead are process-wide settings (skinny_set_pdl, skinny_set_l2_prefetch)
  *    that the _ex entry points override per call (skinny_launch_opts), so code
- *    that wants its own settings never changes what other threads' calls see.
+ *    that wants its own settings never changes what other threads' calls see;
+ *    the decode GEMM's prefetch after a reduce is a per-call setting only.
+ *    None of them changes a result bit.
  *  - Calls are thread-safe on the host.
  */
 #ifndef SKINNY_H
@@ -248,7 +253,9 @@ SKINNY_API int reduce_residual_rmsnorm_ex(const void *partials, int TP, const vo
  *                 any input or between outputs.
  *   All pointers 16-byte aligned. 1 <= M <= 64; 1 <= TP <= 8; K >= 8 and
  *   K % 8 == 0; eps > 0, finite. Needs at least 56 SMs. Uses the decode GEMM's
- *   per-device scratch, like decode_gemm_bf16 (same rules on streams).
+ *   per-device scratch, like decode_gemm_bf16 (same rules on streams). Its
+ *   reduce also raises the signal a following decode GEMM's l2_after_reduce
+ *   waits for (see skinny_launch_opts), and its GEMM lowers it.
  *   Errors: SKINNY_ERR_NULL, _SHAPE, _ALIGN, _ALIAS, _ARG, _DEVICE, _CAPTURE,
  *   _ALLOC, _LAUNCH, _TIMEOUT (as decode_gemm_bf16).
  */
