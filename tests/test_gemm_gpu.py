@@ -270,3 +270,32 @@ def test_gemm_wide_whole_tiles_every_element(cuda_ok, M, N, K, offset):
     sk.decode_gemm_bf16(x, W, other)
     torch.cuda.synchronize()
     assert torch.equal(other.view(torch.int16), out.view(torch.int16))
+
+
+# Shapes drawn once from a seeded generator (random.Random(20261203): M from the
+# row classes, N from four ranges biased to ragged sizes and to the plans near
+# and past one tile per SM, K any multiple of 8 up to 20000), kept as a literal
+# list so that every run checks the same ones.
+RANDOM_SHAPES = [(8, 15167, 2808), (8, 20129, 1240), (24, 142, 3952), (48, 95, 19568),
+                 (32, 20153, 1360), (3, 290, 2704), (1, 3529, 7328), (16, 1674, 5496),
+                 (32, 107, 6120), (1, 1339, 10848), (32, 93, 2456), (64, 22, 15256),
+                 (2, 18242, 13848), (33, 129, 4760), (13, 1184, 17968), (31, 257, 3936),
+                 (13, 264, 10400), (64, 6, 16072), (5, 11480, 16888), (16, 143, 464),
+                 (3, 8205, 16384), (2, 20482, 19592), (5, 19689, 1688), (3, 17828, 4088)]
+
+
+@pytest.mark.parametrize("i", range(len(RANDOM_SHAPES)))
+def test_gemm_random_shapes_every_element(cuda_ok, i):
+    """Every element of each shape against the oracle, with and without PDL and
+    with the output rows 16-byte aligned or not (every second shape starts one
+    element into its buffer), so that the plans, both rings and both store
+    paths meet ragged sizes they are not tuned for."""
+    M, N, K = RANDOM_SHAPES[i]
+    x, W = gemm_inputs_device(M, N, K, workloads.seed_for("random", M, N, K))
+    offset = i % 2
+    buf = torch.empty(M * N + offset, dtype=torch.bfloat16, device="cuda")
+    out = buf[offset:].view(M, N)
+    sk.decode_gemm_bf16(x, W, out, pdl=bool(i % 3 == 0))
+    torch.cuda.synchronize()
+    assert sk.device_error() == (0, 0)
+    check_gemm_full(x, W, out)
