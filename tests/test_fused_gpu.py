@@ -124,3 +124,35 @@ def test_fused_interleaved_with_plain_calls(cuda_ok):
         sk.set_pdl(prev)
     for o in outs:
         assert same_bits(o, alone)
+
+
+# Cases drawn once from a seeded generator (random.Random(7168): M from the row
+# classes, K any multiple of 8 up to 19200, TP in 1..8, a residual or not), kept
+# literal so that every run checks the same ones.
+RANDOM_CASES = [(33, 10040, 6, True), (41, 9192, 8, True), (2, 4040, 6, True),
+                (16, 9616, 6, False), (17, 11760, 7, True), (57, 12000, 7, True),
+                (64, 14832, 6, False), (17, 6240, 5, True), (23, 10608, 5, False),
+                (23, 6968, 4, True), (16, 8264, 4, True), (33, 13320, 3, True),
+                (32, 16704, 5, True), (23, 1088, 7, False), (9, 32, 5, False),
+                (32, 17128, 7, False)]
+
+
+@pytest.mark.parametrize("i", range(len(RANDOM_CASES)))
+def test_fused_random_cases_equal_two_calls(cuda_ok, i):
+    """The fused call against the two calls it replaces, bit for bit (slots,
+    residual_out, out), with PDL on every second case; residual_out against the
+    oracle on the GPU's own slot 0."""
+    M, K, TP, res = RANDOM_CASES[i]
+    x, W, partials, residual, gamma = inputs(M, K, TP, res, 100 + i)
+    prev = sk.set_pdl(i % 2 == 1)
+    try:
+        pu = partials.clone()
+        out_u, rout_u = run_two_calls(x, W, pu, residual, gamma)
+        pf = partials.clone()
+        out_f, rout_f = run_fused(x, W, pf, residual, gamma)
+    finally:
+        sk.set_pdl(prev)
+    assert same_bits(pf, pu) and same_bits(rout_f, rout_u) and same_bits(out_f, out_u)
+    want_h = oracle.reduce_residual(workloads.bits(pf),
+                                    None if residual is None else workloads.bits(residual))
+    assert compare.first_mismatch(workloads.bits(rout_f), want_h) is None
