@@ -77,3 +77,21 @@ def test_logits_rejects_bad_arguments(cuda_ok):
     assert f(x.data_ptr(), W.data_ptr(), out.data_ptr(), 4, 16, 64, 0, 0.0, 1.0, None) == 2
     assert f(x.data_ptr(), W.data_ptr(), out.data_ptr(), 4, 16, 64, 8, float("nan"), 1.0, None) == 10
     assert f(x.data_ptr(), W.data_ptr(), out.data_ptr(), 4, 16, 64, 8, 0.0, float("inf"), None) == 10
+
+
+# Cases drawn once from a seeded generator (random.Random(20480): M from the row
+# classes, N and n_out <= N any, K any multiple of 8 up to 9600, a cap of 0, 1,
+# 5 or 30, a scale of 1, 0.5, -0.25 or 2), kept literal.
+RANDOM_LOGITS = [(3, 16243, 776, 695, 0.0, 0.5), (64, 1791, 2976, 1534, 0.0, 1.0),
+                 (1, 7103, 2936, 5327, 1.0, 0.5), (3, 14649, 8816, 2591, 5.0, 1.0),
+                 (32, 15619, 304, 8576, 0.0, 2.0), (64, 231, 7672, 23, 1.0, 0.5),
+                 (3, 12435, 1560, 9775, 30.0, 1.0), (1, 14338, 2296, 5809, 0.0, 1.0),
+                 (3, 2608, 8656, 2087, 30.0, 1.0), (8, 18002, 1544, 15828, 0.0, 1.0)]
+
+
+@pytest.mark.parametrize("M,N,K,n_out,cap,scale", RANDOM_LOGITS)
+def test_logits_random_cases_every_element(cuda_ok, M, N, K, n_out, cap, scale):
+    x, W = gemm_inputs_device(M, N, K, workloads.seed_for("logits random", M, N, K))
+    x = (x.float() * 8).to(torch.bfloat16)
+    got = run_logits(x, W, n_out, cap, scale)
+    check(x, W[:n_out], workloads.bits(got), cap, scale)
