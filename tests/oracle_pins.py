@@ -61,7 +61,8 @@ def bf16_bits_of(values) -> np.ndarray:
 
 def bits_to_f64(b) -> np.ndarray:
     u = np.asarray(b, dtype=np.uint16).astype(np.uint32) << 16
-    return u.view(np.float32).astype(np.float64)
+    with np.errstate(invalid="ignore"):  # NaN patterns stay NaN
+        return u.view(np.float32).astype(np.float64)
 
 
 def random_bf16(rng, shape, std=1.0) -> np.ndarray:

@@ -27,11 +27,14 @@ def _with(**overrides):
 
 
 def _round_via_f32(v):
-    return f32_to_bf16_torch(np.asarray(v, dtype=np.float64).astype(np.float32))
+    with np.errstate(over="ignore"):  # out-of-range values become infinities
+        f = np.asarray(v, dtype=np.float64).astype(np.float32)
+    return f32_to_bf16_torch(f)
 
 
 def _round_truncate(v):
-    f = np.asarray(v, dtype=np.float64).astype(np.float32)
+    with np.errstate(over="ignore"):  # out-of-range values become infinities
+        f = np.asarray(v, dtype=np.float64).astype(np.float32)
     return (f.view(np.uint32) >> 16).astype(np.uint16)
 
 
