@@ -791,6 +791,7 @@ def main():
         for _ in range(3):
             fn()
         torch.cuda.synchronize()
+        host_lead(stream)
         e0.record(stream)
         for _ in range(reps):
             fn()
